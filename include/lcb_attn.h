@@ -1,0 +1,211 @@
+/*
+ * lcb_attn.h — C ABI of the blockwise causal attention library (libattn.so).
+ *
+ * Exact softmax attention, forward and backward, computed tile by tile with an
+ * online softmax on GB300 (sm_103a) tensor cores, plus the two pieces that
+ * ring and zigzag-ring sequence parallelism add on top of it: merging partial
+ * results by log-sum-exp and the zigzag split/schedule.
+ *
+ * Sources (web pages on EasyContext, cited by title and section):
+ *  [FA]  "EasyContext核心技术解析：序列并行与Flash Attention的完美结合",
+ *        §2 "Flash Attention优化": exact attention computed in blocks with
+ *        recomputation, never storing the full score matrix; the block
+ *        forward/backward entry points of Flash Attention.
+ *  [SP]  same page, §1 "序列并行技术": ring attention over sequence shards.
+ *  [ZZ]  "EasyContext代码解析200行核心训练脚本实现原理", §模型并行策略解析
+ *        (zigzag_ring_attn) and §训练循环核心逻辑 (prepare_seq_parallel_inputs
+ *        splits each sequence into rank-local pieces).
+ *  [FULL] "EasyContext：用最少资源扩展大模型至百万Token": full attention.
+ *
+ * Conventions shared by every entry point
+ *  - Tensors Q, K, V, O, dO, dQ, dK, dV are [B, S, H, D] (token-major, heads
+ *    interleaved in a row), bf16 unless stated; D must be 128. LSE and Delta
+ *    are fp32 [B, H, S].
+ *  - LSE is the natural log of sum_j exp(scale * q . k_j) over visible keys
+ *    (scale included); -inf for a row with no visible key.
+ *  - causal: key j is visible to query i iff j <= i (requires Sq == Sk).
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    keeps no pointer after a call returns and allocates nothing.
+ *  - stream is a cudaStream_t (NULL = legacy default stream). Every compute
+ *    call only enqueues work and returns; results are ready when the stream
+ *    reaches that point.
+ *  - Device pointers must be 16-byte aligned and strides multiples of 8
+ *    elements (16 bytes), as required by the tensor-memory-access (TMA) unit.
+ *  - Return value: LCB_OK or a negative LCB_ERR_* code; nothing is launched on
+ *    an argument error. With the environment variable LCB_CHECKED=1 every call
+ *    synchronises its stream and reports LCB_ERR_TIMEOUT if a kernel's
+ *    bounded wait expired (the kernel then returned early, outputs undefined).
+ */
+#ifndef LCB_ATTN_H
+#define LCB_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LCB_OK 0
+#define LCB_ERR_ARG (-1)         /* null pointer, bad size, misaligned pointer or stride */
+#define LCB_ERR_UNSUPPORTED (-2) /* D != 128, causal with Sq != Sk, unknown dtype */
+#define LCB_ERR_SCHEDULE (-3)    /* zigzag: P < 1 or S not a positive multiple of 2P */
+#define LCB_ERR_CUDA (-4)        /* a CUDA runtime/driver call or launch failed */
+#define LCB_ERR_TIMEOUT (-5)     /* checked mode: a device-side bounded wait expired */
+
+#define LCB_DTYPE_BF16 0
+#define LCB_DTYPE_F32 1
+
+/* How attn_bwd_ex writes dq/dk/dv. */
+#define LCB_GRAD_BF16 0      /* bf16, overwritten */
+#define LCB_GRAD_F32_ACCUM 1 /* fp32, the block's contribution is added */
+#define LCB_GRAD_F32_STORE 2 /* fp32, overwritten */
+
+#define LCB_TASK_DIAG 0
+#define LCB_TASK_LOWER 1
+#define LCB_TASK_UPPER 2
+
+/* One attention task of the zigzag ring: rank `rank` at ring step `step`
+ * attends its queries [q_off, q_off+q_len) to the keys/values it holds from
+ * rank `src`, [k_off, k_off+k_len); offsets are rows in zigzag order. */
+typedef struct lcb_task {
+  int32_t rank, step, src, kind;
+  int32_t q_off, q_len, k_off, k_len;
+  int32_t causal;
+} lcb_task;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* attn_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int lcb_version(void);
+
+/*
+ * attn_fwd — causal (or full) attention forward, [FA] §2, [FULL].
+ *   O_i = sum_j softmax_j(scale * q_i . k_j) v_j,  LSE_i as above.
+ * q, k, v: [B,S,H,D] bf16 (in); o: [B,S,H,D] bf16 (out); lse: [B,H,S] fp32
+ * (out). Contiguous layouts. S may be any positive size (ragged tails are
+ * masked); causal is 0 or 1; scale > 0 (normally 1/sqrt(D)).
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int D,
+             int causal, float scale, void* stream);
+
+/*
+ * attn_fwd_ex — forward on strided views, for ring steps ([SP], [ZZ]).
+ * Queries have Sq rows, keys/values Sk rows (Sq != Sk only when causal == 0).
+ * Strides are in elements: row stride between consecutive tokens, batch stride
+ * between batches; q and o share nothing but shape. o_dtype selects bf16 or
+ * fp32 output. lse strides: between heads and between batches.
+ * Sk == 0 writes O = 0 and LSE = -inf.
+ */
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk,
+                int D, int causal, float scale, long long q_row_stride, long long q_batch_stride,
+                long long kv_row_stride, long long kv_batch_stride, long long o_row_stride,
+                long long o_batch_stride, int o_dtype, long long lse_head_stride, long long lse_batch_stride,
+                void* stream);
+
+/* Bytes of device workspace attn_bwd needs (Delta, fp32 [B,H,S]). */
+size_t attn_bwd_workspace_bytes(int B, int H, int S, int D);
+
+/*
+ * attn_bwd — backward of attn_fwd with recomputation, [FA] §2 ("重新计算").
+ * Inputs q, k, v, o, dO bf16 [B,S,H,D] and lse fp32 [B,H,S] as returned by
+ * attn_fwd; outputs dq, dk, dv bf16 [B,S,H,D] (overwritten). Runs the
+ * Delta = rowsum(dO * O) preprocess, then a dK/dV pass and a dQ pass.
+ * workspace: device memory of at least attn_bwd_workspace_bytes(), 16-byte
+ * aligned, owned by the caller, contents ignored.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+             void* dq, void* dk, void* dv, int B, int H, int S, int D, int causal, float scale, void* workspace,
+             size_t ws_bytes, void* stream);
+
+/*
+ * attn_bwd_preprocess — Delta_i = sum_d dO_id * O_id in fp32 (the per-row
+ * term of dS = P * (dP - Delta)). o, dO bf16 [B,S,H,D] views with the given
+ * row/batch strides (elements); delta fp32 with head/batch strides.
+ */
+int attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H, int S, int D,
+                        long long row_stride, long long batch_stride, long long delta_head_stride,
+                        long long delta_batch_stride, void* stream);
+
+/*
+ * attn_bwd_ex — backward of one block of keys with the row statistics given,
+ * for ring steps ([SP], [ZZ]): P_ij = exp(scale q_i.k_j - LSE_i),
+ * dS_ij = P_ij (dO_i.v_j - Delta_i). lse and delta ([B,H,Sq] with the given
+ * strides) are the statistics over ALL keys of the full problem, so gradients
+ * of disjoint key blocks add up to the monolithic gradient.
+ * grad_mode LCB_GRAD_BF16: dq/dk/dv are bf16 and overwritten.
+ * grad_mode LCB_GRAD_F32_ACCUM: dq/dk/dv are fp32 and the block's
+ *   contribution is ADDED to them (read-modify-write; calls on one stream
+ *   never race, calls on different streams touching the same rows do).
+ * grad_mode LCB_GRAD_F32_STORE: dq/dk/dv are fp32 and overwritten.
+ * Gradient strides: dq uses dq_row/batch strides, dk and dv share dkv strides
+ * (elements of the gradient dtype).
+ */
+int attn_bwd_ex(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                const void* dO, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, int causal,
+                float scale, long long q_row_stride, long long q_batch_stride, long long kv_row_stride,
+                long long kv_batch_stride, long long lse_head_stride, long long lse_batch_stride, int grad_mode,
+                long long dq_row_stride, long long dq_batch_stride, long long dkv_row_stride,
+                long long dkv_batch_stride, void* stream);
+
+/*
+ * attn_lse_merge — fold a partial result into an accumulator, [SP]:
+ *   m = max(L_acc, L_b), w_x = exp(L_x - m),
+ *   L_acc <- m + ln(w_acc + w_b),  O_acc <- (w_acc O_acc + w_b O_b)/(w_acc + w_b)
+ * Both sides -inf gives L = -inf, O = 0. o_acc fp32 and o_b (bf16 or fp32 per
+ * o_b_dtype) are [B, rows, H, D] views with the same strides (elements);
+ * lse_acc and lse_b are fp32 [B, H, rows] views with the same strides.
+ * If o_out_bf16 is not NULL the merged O is also written there as bf16 (same
+ * strides), which ends a ring without a separate cast.
+ */
+int attn_lse_merge(float* o_acc, float* lse_acc, const void* o_b, const float* lse_b, int o_b_dtype,
+                   void* o_out_bf16, int B, int H, int rows, int D, long long o_row_stride, long long o_batch_stride,
+                   long long lse_head_stride, long long lse_batch_stride, void* stream);
+
+/*
+ * zigzag_schedule — the zigzag split and ring task table, [ZZ]. HOST memory.
+ * c = S / (2P); rank r holds chunks r and 2P-1-r (in that order); perm[t]
+ * (t < S) is the natural token index at zigzag position t. tasks[r*P + s]
+ * (P*P entries) is rank r's task at ring step s, src = (r - s) mod P:
+ * DIAG (s = 0): local x local, causal; LOWER (src < r): 2c local queries x
+ * src's first chunk; UPPER (src > r): local second chunk x src's 2c keys.
+ * Either output pointer may be NULL. Returns LCB_ERR_SCHEDULE on bad S, P.
+ */
+int zigzag_schedule(int S, int P, int* perm, lcb_task* tasks);
+
+/*
+ * lcb_permute_rows — row gather/scatter on the device, used to move a
+ * [B=1, S, H, D] tensor into zigzag order and back, [ZZ].
+ * scatter == 0: dst[t] = src[perm[t]];  scatter == 1: dst[perm[t]] = src[t].
+ * perm: DEVICE int32 [rows]; row_bytes a multiple of 16; src != dst.
+ */
+int lcb_permute_rows(const void* src, void* dst, const int* perm, int rows, long long row_bytes, void* stream);
+int lcb_scatter_rows(const void* src, void* dst, const int* perm, int rows, long long row_bytes, void* stream);
+
+/* lcb_cast_f32_bf16 — dst[i] = bf16(src[i]) (round to nearest even) for
+ * i < n; ends a ring whose accumulators are fp32. Both 16-byte aligned. */
+int lcb_cast_f32_bf16(const float* src, void* dst, long long n, void* stream);
+
+/* Bounded-wait limit of all kernels, nanoseconds (default 2e9, or the
+ * environment variable LCB_WAIT_LIMIT_NS). Returns the previous value. */
+unsigned long long lcb_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * lcb_selftest_bounded_wait — launches a one-CTA kernel that waits on a
+ * barrier nothing ever completes, with the current wait limit, synchronises
+ * the stream and returns the outcome: LCB_ERR_TIMEOUT when the wait expired
+ * and the kernel returned cleanly (the expected result), LCB_OK if it did not
+ * expire, LCB_ERR_CUDA on a CUDA failure. Clears the status word afterwards.
+ */
+int lcb_selftest_bounded_wait(void* stream);
+
+/* Reads and clears the device status word of the current device (a
+ * synchronising call): 0, or a bitmask with 1 = a bounded wait expired. */
+int lcb_take_device_status(unsigned int* where);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCB_ATTN_H */

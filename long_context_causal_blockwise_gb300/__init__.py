@@ -1,0 +1,31 @@
+"""Blockwise causal attention for GB300 (sm_103a): the hot path of long-context
+training with sequence parallelism, as a C-ABI CUDA library (libattn.so) with a
+thin Python binding.
+
+Public calls (all run in this library's CUDA kernels):
+  attn_fwd, attn_fwd_ex, attn_bwd, attn_bwd_ex, attn_bwd_preprocess,
+  attn_lse_merge, zigzag_schedule, permute_rows, cast_f32_bf16,
+  zigzag_attention_fwd / zigzag_attention_bwd (the one-device zigzag ring).
+
+The shared library is loaded on first use; importing the package does not
+touch the GPU.
+"""
+
+from ._lib import (  # noqa: F401
+    AttnError,
+    attn_bwd,
+    attn_bwd_ex,
+    attn_bwd_preprocess,
+    attn_bwd_workspace_bytes,
+    attn_fwd,
+    attn_fwd_ex,
+    attn_lse_merge,
+    cast_f32_bf16,
+    load,
+    permute_rows,
+    selftest_bounded_wait,
+    set_wait_limit_ns,
+    take_device_status,
+    zigzag_schedule,
+)
+from .zigzag import zigzag_attention_bwd, zigzag_attention_fwd  # noqa: F401

@@ -1,0 +1,302 @@
+"""ctypes binding of libattn.so (include/lcb_attn.h).
+
+Argument marshalling only: torch tensors are passed as device pointers with
+their strides, and the current CUDA stream is passed as the stream. Every step
+of the computation runs in the library's CUDA kernels; if the library cannot be
+loaded, every call raises (there is no fallback).
+"""
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+LCB_OK = 0
+LCB_ERR_ARG = -1
+LCB_ERR_UNSUPPORTED = -2
+LCB_ERR_SCHEDULE = -3
+LCB_ERR_CUDA = -4
+LCB_ERR_TIMEOUT = -5
+LCB_DTYPE_BF16 = 0
+LCB_DTYPE_F32 = 1
+LCB_GRAD_BF16 = 0
+LCB_GRAD_F32_ACCUM = 1
+LCB_GRAD_F32_STORE = 2
+TASK_DIAG, TASK_LOWER, TASK_UPPER = 0, 1, 2
+
+
+class LcbTask(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("rank", "step", "src", "kind", "q_off", "q_len", "k_off", "k_len", "causal")]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn} failed: {msg} ({status})")
+        self.status = status
+
+
+_LIB = None
+
+_P, _I, _F, _LL, _SZ, _U64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong,
+                               ctypes.c_size_t, ctypes.c_ulonglong)
+
+_SIGNATURES = {
+    "attn_status_string": ([_I], ctypes.c_char_p),
+    "lcb_version": ([], _I),
+    "attn_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P], _I),
+    "attn_fwd_ex": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _I, _LL, _LL, _P],
+                    _I),
+    "attn_bwd_workspace_bytes": ([_I, _I, _I, _I], _SZ),
+    "attn_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P], _I),
+    "attn_bwd_preprocess": ([_P, _P, _P, _I, _I, _I, _I, _LL, _LL, _LL, _LL, _P], _I),
+    "attn_bwd_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _I,
+                     _LL, _LL, _LL, _LL, _P], _I),
+    "attn_lse_merge": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _LL, _LL, _LL, _LL, _P], _I),
+    "zigzag_schedule": ([_I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(LcbTask)], _I),
+    "lcb_permute_rows": ([_P, _P, _P, _I, _LL, _P], _I),
+    "lcb_scatter_rows": ([_P, _P, _P, _I, _LL, _P], _I),
+    "lcb_cast_f32_bf16": ([_P, _P, _LL, _P], _I),
+    "lcb_set_wait_limit_ns": ([_U64], _U64),
+    "lcb_selftest_bounded_wait": ([_P], _I),
+    "lcb_take_device_status": ([ctypes.POINTER(ctypes.c_uint)], _I),
+}
+
+EXPORTED = tuple(_SIGNATURES)
+
+
+def lib_path():
+    return _build.LIB
+
+
+def load(build_if_missing=True):
+    """Loads (building first if needed) and returns the ctypes library."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.LIB
+    if build_if_missing and (_build.needs_build()):
+        _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libattn.so not found at {path}; run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _LIB = lib
+    return lib
+
+
+def _check(fn, status):
+    if status != LCB_OK:
+        msg = load().attn_status_string(status).decode()
+        raise AttnError(fn, status, msg)
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, ndim):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name} must be contiguous in its last dim")
+
+
+def _bshd(t, name, dtype=torch.bfloat16):
+    """(row_stride, batch_stride) of a [B,S,H,D] view whose [H,D] part is dense."""
+    _need(t, dtype, name, 4)
+    B, S, H, D = t.shape
+    if t.stride(2) != D:
+        raise ValueError(f"{name}: heads must be dense within a row")
+    return t.stride(1), t.stride(0)
+
+
+def _bhs(t, name):
+    _need(t, torch.float32, name, 3)
+    return t.stride(1), t.stride(0)
+
+
+# ------------------------------------------------------------------ forward
+
+def attn_fwd(q, k, v, causal=True, scale=None, o=None, lse=None):
+    """Contiguous [B,S,H,D] bf16 forward; returns (o bf16, lse fp32 [B,H,S])."""
+    B, S, H, D = q.shape
+    scale = D ** -0.5 if scale is None else scale
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _need(t, torch.bfloat16, n, 4)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous (use attn_fwd_ex for strided views)")
+    if not lse.is_contiguous():
+        raise ValueError("lse must be contiguous")
+    _check("attn_fwd", load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, S, D, int(causal),
+                                       float(scale), _stream(q)))
+    return o, lse
+
+
+def attn_fwd_ex(q, k, v, o, lse, causal, scale):
+    """Forward on strided [B,S,H,D] views; o bf16 or fp32; lse [B,H,Sq] view."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    qr, qb = _bshd(q, "q")
+    kr, kb = _bshd(k, "k")
+    vr, vb = _bshd(v, "v")
+    if (vr, vb) != (kr, kb):
+        raise ValueError("k and v must share strides")
+    o_dtype = LCB_DTYPE_F32 if o.dtype == torch.float32 else LCB_DTYPE_BF16
+    orr, ob = _bshd(o, "o", o.dtype)
+    lh, lb = _bhs(lse, "lse")
+    _check("attn_fwd_ex", load().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk, D,
+                                             int(causal), float(scale), qr, qb, kr, kb, orr, ob, o_dtype, lh, lb,
+                                             _stream(q)))
+    return o, lse
+
+
+# ------------------------------------------------------------------ backward
+
+def attn_bwd_workspace_bytes(B, H, S, D=128):
+    return int(load().attn_bwd_workspace_bytes(B, H, S, D))
+
+
+def attn_bwd(q, k, v, o, lse, do, causal=True, scale=None, dq=None, dk=None, dv=None, workspace=None):
+    """Contiguous backward; returns (dq, dk, dv) bf16."""
+    B, S, H, D = q.shape
+    scale = D ** -0.5 if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, torch.bfloat16, n, 4)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    ws_bytes = attn_bwd_workspace_bytes(B, H, S, D)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _check("attn_bwd", load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                                       _ptr(dv), B, H, S, D, int(causal), float(scale), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(q)))
+    return dq, dk, dv
+
+
+def attn_bwd_preprocess(o, do, delta):
+    B, S, H, D = o.shape
+    r, b = _bshd(o, "o")
+    if _bshd(do, "do") != (r, b):
+        raise ValueError("o and do must share strides")
+    dh, db = _bhs(delta, "delta")
+    _check("attn_bwd_preprocess", load().attn_bwd_preprocess(_ptr(o), _ptr(do), _ptr(delta), B, H, S, D, r, b, dh,
+                                                             db, _stream(o)))
+    return delta
+
+
+def attn_bwd_ex(q, k, v, lse, delta, do, dq, dk, dv, causal, scale, accumulate=True):
+    """Block backward with given row statistics.
+
+    bf16 gradients are overwritten; fp32 gradients are accumulated into
+    (accumulate=True) or overwritten (accumulate=False)."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    qr, qb = _bshd(q, "q")
+    if _bshd(do, "do") != (qr, qb):
+        raise ValueError("q and do must share strides")
+    kr, kb = _bshd(k, "k")
+    if _bshd(v, "v") != (kr, kb):
+        raise ValueError("k and v must share strides")
+    lh, lb = _bhs(lse, "lse")
+    if _bhs(delta, "delta") != (lh, lb):
+        raise ValueError("lse and delta must share strides")
+    gdt = dq.dtype
+    if dk.dtype != gdt or dv.dtype != gdt:
+        raise ValueError("dq, dk, dv must share a dtype")
+    if gdt == torch.float32:
+        grad_mode = LCB_GRAD_F32_ACCUM if accumulate else LCB_GRAD_F32_STORE
+    else:
+        grad_mode = LCB_GRAD_BF16
+    dqr, dqb = _bshd(dq, "dq", gdt)
+    dkr, dkb = _bshd(dk, "dk", gdt)
+    if _bshd(dv, "dv", gdt) != (dkr, dkb):
+        raise ValueError("dk and dv must share strides")
+    _check("attn_bwd_ex", load().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(do), _ptr(dq),
+                                             _ptr(dk), _ptr(dv), B, H, Sq, Sk, D, int(causal), float(scale), qr, qb,
+                                             kr, kb, lh, lb, grad_mode, dqr, dqb, dkr, dkb, _stream(q)))
+    return dq, dk, dv
+
+
+# ------------------------------------------------------------------ merge / zigzag
+
+def attn_lse_merge(o_acc, lse_acc, o_b, lse_b, o_out_bf16=None):
+    """In-place (o_acc fp32, lse_acc) <- merge with (o_b, lse_b)."""
+    B, R, H, D = o_acc.shape
+    r, b = _bshd(o_acc, "o_acc", torch.float32)
+    if _bshd(o_b, "o_b", o_b.dtype) != (r, b):
+        raise ValueError("o_acc and o_b must share strides")
+    lh, lb = _bhs(lse_acc, "lse_acc")
+    if _bhs(lse_b, "lse_b") != (lh, lb):
+        raise ValueError("lse_acc and lse_b must share strides")
+    if o_out_bf16 is not None and _bshd(o_out_bf16, "o_out_bf16") != (r, b):
+        raise ValueError("o_out_bf16 must share o_acc's strides")
+    odt = LCB_DTYPE_F32 if o_b.dtype == torch.float32 else LCB_DTYPE_BF16
+    _check("attn_lse_merge", load().attn_lse_merge(_ptr(o_acc), _ptr(lse_acc), _ptr(o_b), _ptr(lse_b), odt,
+                                                   None if o_out_bf16 is None else _ptr(o_out_bf16), B, H, R, D, r,
+                                                   b, lh, lb, _stream(o_acc)))
+    return o_acc, lse_acc
+
+
+def zigzag_schedule(S, P):
+    """Host call: returns (perm list[int], tasks list[dict])."""
+    perm = (ctypes.c_int * S)()
+    tasks = (LcbTask * (P * P))()
+    _check("zigzag_schedule", load().zigzag_schedule(S, P, perm, tasks))
+    return list(perm), [{f: getattr(t, f) for f, _ in LcbTask._fields_} for t in tasks]
+
+
+def permute_rows(src, dst, perm_dev, scatter=False):
+    """Rows of contiguous [1, S, ...] tensors: dst[t] = src[perm[t]] (or the scatter)."""
+    if not (src.is_contiguous() and dst.is_contiguous()) or src.shape != dst.shape or src.dtype != dst.dtype:
+        raise ValueError("src and dst must be contiguous tensors of one shape and dtype")
+    if perm_dev.dtype != torch.int32 or not perm_dev.is_cuda:
+        raise ValueError("perm must be a CUDA int32 tensor")
+    rows = perm_dev.numel()
+    row_bytes = src.numel() // rows * src.element_size()
+    fn = load().lcb_scatter_rows if scatter else load().lcb_permute_rows
+    _check("permute_rows", fn(_ptr(src), _ptr(dst), _ptr(perm_dev), rows, row_bytes, _stream(src)))
+    return dst
+
+
+def cast_f32_bf16(src, dst):
+    if src.dtype != torch.float32 or dst.dtype != torch.bfloat16 or src.numel() != dst.numel():
+        raise ValueError("cast_f32_bf16 wants fp32 src and bf16 dst of one size")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("cast_f32_bf16 wants contiguous tensors")
+    _check("lcb_cast_f32_bf16", load().lcb_cast_f32_bf16(_ptr(src), _ptr(dst), src.numel(), _stream(src)))
+    return dst
+
+
+def set_wait_limit_ns(ns):
+    return int(load().lcb_set_wait_limit_ns(int(ns)))
+
+
+def selftest_bounded_wait():
+    return int(load().lcb_selftest_bounded_wait(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
+
+
+def take_device_status():
+    where = ctypes.c_uint(0)
+    bits = load().lcb_take_device_status(ctypes.byref(where))
+    return int(bits), int(where.value)

@@ -1,0 +1,420 @@
+// C ABI of libattn.so: argument validation, TMA descriptor set-up, status
+// handling and the host-side zigzag schedule. Every compute entry point
+// enqueues kernels of this library on the caller's stream; there is no other
+// backend and no CPU fallback.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "lcb_attn.h"
+#include "lcb_internal.h"
+
+namespace lcb {
+namespace {
+
+constexpr int kHeadDim = 128;
+constexpr int kMaxDevices = 64;
+
+__device__ uint32_t g_status_words[4];
+
+uint32_t* g_status_ptr[kMaxDevices] = {};
+std::mutex g_mu;
+
+unsigned long long env_wait_limit() {
+  const char* s = std::getenv("LCB_WAIT_LIMIT_NS");
+  if (s && *s) {
+    const unsigned long long v = std::strtoull(s, nullptr, 10);
+    if (v > 0) return v;
+  }
+  return 2000000000ULL;
+}
+
+std::atomic<unsigned long long> g_wait_limit{env_wait_limit()};
+
+bool checked_mode() {
+  static const bool on = [] {
+    const char* s = std::getenv("LCB_CHECKED");
+    return s && s[0] == '1';
+  }();
+  return on;
+}
+
+// Device address of the status word on the current device (set-up once per device).
+int status_words(uint32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LCB_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_words) != cudaSuccess) return LCB_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return LCB_OK;
+}
+
+int dev_status(DevStatus* st) {
+  uint32_t* w = nullptr;
+  const int rc = status_words(&w);
+  if (rc != LCB_OK) return rc;
+  st->words = w;
+  st->limit = g_wait_limit.load();
+  return LCB_OK;
+}
+
+// Reads and clears the status word (synchronous).
+int take_status(uint32_t* bits, uint32_t* where) {
+  uint32_t w[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(w, g_status_words, sizeof(w)) != cudaSuccess) return LCB_ERR_CUDA;
+  if (w[0] != 0) {
+    const uint32_t z[4] = {0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(g_status_words, z, sizeof(z)) != cudaSuccess) return LCB_ERR_CUDA;
+  }
+  *bits = w[0];
+  if (where) *where = w[1];
+  return LCB_OK;
+}
+
+int finish(int rc, cudaStream_t stream) {
+  if (rc != LCB_OK) return rc;
+  if (!checked_mode()) return LCB_OK;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return LCB_ERR_CUDA;
+  uint32_t bits = 0;
+  if ((rc = take_status(&bits, nullptr)) != LCB_OK) return rc;
+  return (bits & DEV_TIMEOUT) ? LCB_ERR_TIMEOUT : LCB_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool stride_ok(long long s) { return s >= 0 && (s % 8) == 0 && s < (1LL << 38); }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+int make_tma_map_bf16(CUtensorMap* map, const RowView& v, int B, int rows, int HD, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return LCB_ERR_CUDA;
+  const long long bstride = (B == 1) ? static_cast<long long>(rows) * v.row_stride : v.batch_stride;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(v.row_stride) * 2, static_cast<cuuint64_t>(bstride) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v.ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LCB_OK : LCB_ERR_ARG;
+}
+
+}  // namespace lcb
+
+using namespace lcb;
+
+extern "C" {
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case LCB_OK: return "ok";
+    case LCB_ERR_ARG: return "invalid argument";
+    case LCB_ERR_UNSUPPORTED: return "unsupported configuration";
+    case LCB_ERR_SCHEDULE: return "invalid zigzag schedule size";
+    case LCB_ERR_CUDA: return "CUDA error";
+    case LCB_ERR_TIMEOUT: return "device bounded wait expired";
+    default: return "unknown status";
+  }
+}
+
+int lcb_version(void) { return 100; }
+
+unsigned long long lcb_set_wait_limit_ns(unsigned long long ns) {
+  if (ns == 0) ns = 1;
+  return g_wait_limit.exchange(ns);
+}
+
+int lcb_take_device_status(unsigned int* where) {
+  uint32_t bits = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return LCB_ERR_CUDA;
+  const int rc = take_status(&bits, where);
+  return rc != LCB_OK ? rc : static_cast<int>(bits);
+}
+
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk,
+                int D, int causal, float scale, long long q_row_stride, long long q_batch_stride,
+                long long kv_row_stride, long long kv_batch_stride, long long o_row_stride,
+                long long o_batch_stride, int o_dtype, long long lse_head_stride, long long lse_batch_stride,
+                void* stream) {
+  if (B < 1 || H < 1 || Sq < 0 || Sk < 0) return LCB_ERR_ARG;
+  if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return LCB_ERR_ARG;
+  if (causal && Sq != Sk) return LCB_ERR_UNSUPPORTED;
+  if (o_dtype != LCB_DTYPE_BF16 && o_dtype != LCB_DTYPE_F32) return LCB_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return LCB_ERR_ARG;
+  if (Sq == 0) return LCB_OK;
+  if (!o || !lse || !aligned16(o)) return LCB_ERR_ARG;
+  if (!stride_ok(o_row_stride) || !stride_ok(o_batch_stride)) return LCB_ERR_ARG;
+  if (lse_head_stride < 0 || lse_batch_stride < 0) return LCB_ERR_ARG;
+  if (static_cast<long long>(H) * kHeadDim > o_row_stride) return LCB_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (Sk == 0) {
+    return finish(launch_fill_empty(o, o_dtype == LCB_DTYPE_F32, o_row_stride, o_batch_stride, lse, lse_head_stride,
+                                    lse_batch_stride, B, H, Sq, st),
+                  st);
+  }
+  if (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v)) return LCB_ERR_ARG;
+  if (!stride_ok(q_row_stride) || !stride_ok(q_batch_stride) || !stride_ok(kv_row_stride) ||
+      !stride_ok(kv_batch_stride))
+    return LCB_ERR_ARG;
+  if (static_cast<long long>(H) * kHeadDim > q_row_stride || static_cast<long long>(H) * kHeadDim > kv_row_stride)
+    return LCB_ERR_ARG;
+  FwdLaunch a;
+  a.q = {q, q_row_stride, q_batch_stride};
+  a.k = {k, kv_row_stride, kv_batch_stride};
+  a.v = {v, kv_row_stride, kv_batch_stride};
+  a.o = o;
+  a.lse = lse;
+  a.o_row_stride = o_row_stride;
+  a.o_batch_stride = o_batch_stride;
+  a.lse_head_stride = lse_head_stride;
+  a.lse_batch_stride = lse_batch_stride;
+  a.B = B;
+  a.H = H;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.causal = causal;
+  a.o_f32 = o_dtype == LCB_DTYPE_F32;
+  a.scale = scale;
+  int rc = dev_status(&a.st);
+  if (rc != LCB_OK) return rc;
+  return finish(launch_attn_fwd(a, st), st);
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int D,
+             int causal, float scale, void* stream) {
+  const long long rs = static_cast<long long>(H) * D;
+  const long long bs = rs * S;
+  return attn_fwd_ex(q, k, v, o, lse, B, H, S, S, D, causal, scale, rs, bs, rs, bs, rs, bs, LCB_DTYPE_BF16, S,
+                     static_cast<long long>(H) * S, stream);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int S, int D) {
+  (void)D;
+  if (B < 1 || H < 1 || S < 0) return 0;
+  const size_t n = static_cast<size_t>(B) * H * S * sizeof(float);
+  return (n + 255) & ~static_cast<size_t>(255);
+}
+
+int attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H, int S, int D,
+                        long long row_stride, long long batch_stride, long long delta_head_stride,
+                        long long delta_batch_stride, void* stream) {
+  if (B < 1 || H < 1 || S < 0) return LCB_ERR_ARG;
+  if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
+  if (S == 0) return LCB_OK;
+  if (!o || !dO || !delta || (reinterpret_cast<uintptr_t>(o) & 7u) || (reinterpret_cast<uintptr_t>(dO) & 7u))
+    return LCB_ERR_ARG;
+  if (row_stride < static_cast<long long>(H) * D || (row_stride % 4) || batch_stride < 0 || (batch_stride % 4))
+    return LCB_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return finish(launch_bwd_preprocess(o, dO, row_stride, batch_stride, delta, delta_head_stride, delta_batch_stride, B,
+                                      H, S, st),
+                st);
+}
+
+int attn_bwd_ex(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                const void* dO, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, int causal,
+                float scale, long long q_row_stride, long long q_batch_stride, long long kv_row_stride,
+                long long kv_batch_stride, long long lse_head_stride, long long lse_batch_stride, int grad_mode,
+                long long dq_row_stride, long long dq_batch_stride, long long dkv_row_stride,
+                long long dkv_batch_stride, void* stream) {
+  if (B < 1 || H < 1 || Sq < 0 || Sk < 0) return LCB_ERR_ARG;
+  if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return LCB_ERR_ARG;
+  if (causal && Sq != Sk) return LCB_ERR_UNSUPPORTED;
+  if (grad_mode != LCB_GRAD_BF16 && grad_mode != LCB_GRAD_F32_ACCUM && grad_mode != LCB_GRAD_F32_STORE)
+    return LCB_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return LCB_ERR_ARG;
+  if (Sq == 0 && Sk == 0) return LCB_OK;
+  if (!q || !k || !v || !lse || !delta || !dO || !dq || !dk || !dv) return LCB_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv))
+    return LCB_ERR_ARG;
+  if (!stride_ok(q_row_stride) || !stride_ok(q_batch_stride) || !stride_ok(kv_row_stride) ||
+      !stride_ok(kv_batch_stride) || !stride_ok(dq_row_stride) || !stride_ok(dq_batch_stride) ||
+      !stride_ok(dkv_row_stride) || !stride_ok(dkv_batch_stride))
+    return LCB_ERR_ARG;
+  const long long HD = static_cast<long long>(H) * kHeadDim;
+  if (HD > q_row_stride || HD > kv_row_stride || HD > dq_row_stride || HD > dkv_row_stride) return LCB_ERR_ARG;
+  if (lse_head_stride < 0 || lse_batch_stride < 0) return LCB_ERR_ARG;
+  BwdLaunch a;
+  a.q = {q, q_row_stride, q_batch_stride};
+  a.dO = {dO, q_row_stride, q_batch_stride};
+  a.k = {k, kv_row_stride, kv_batch_stride};
+  a.v = {v, kv_row_stride, kv_batch_stride};
+  a.lse = lse;
+  a.delta = delta;
+  a.lse_head_stride = lse_head_stride;
+  a.lse_batch_stride = lse_batch_stride;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dq_row_stride = dq_row_stride;
+  a.dq_batch_stride = dq_batch_stride;
+  a.dkv_row_stride = dkv_row_stride;
+  a.dkv_batch_stride = dkv_batch_stride;
+  a.B = B;
+  a.H = H;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.causal = causal;
+  a.grad_mode = grad_mode;
+  a.scale = scale;
+  int rc = dev_status(&a.st);
+  if (rc != LCB_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (Sk > 0) {
+    if ((rc = launch_attn_bwd_dkdv(a, st)) != LCB_OK) return rc;
+  }
+  if (Sq > 0) {
+    if ((rc = launch_attn_bwd_dq(a, st)) != LCB_OK) return rc;
+  }
+  return finish(LCB_OK, st);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+             void* dq, void* dk, void* dv, int B, int H, int S, int D, int causal, float scale, void* workspace,
+             size_t ws_bytes, void* stream) {
+  if (B < 1 || H < 1 || S < 0) return LCB_ERR_ARG;
+  if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
+  if (S == 0) return LCB_OK;
+  if (!workspace || !aligned16(workspace) || ws_bytes < attn_bwd_workspace_bytes(B, H, S, D)) return LCB_ERR_ARG;
+  const long long rs = static_cast<long long>(H) * D;
+  const long long bs = rs * S;
+  float* delta = static_cast<float*>(workspace);
+  int rc = attn_bwd_preprocess(o, dO, delta, B, H, S, D, rs, bs, S, static_cast<long long>(H) * S, stream);
+  if (rc != LCB_OK) return rc;
+  return attn_bwd_ex(q, k, v, lse, delta, dO, dq, dk, dv, B, H, S, S, D, causal, scale, rs, bs, rs, bs, S,
+                     static_cast<long long>(H) * S, LCB_GRAD_BF16, rs, bs, rs, bs, stream);
+}
+
+int attn_lse_merge(float* o_acc, float* lse_acc, const void* o_b, const float* lse_b, int o_b_dtype,
+                   void* o_out_bf16, int B, int H, int rows, int D, long long o_row_stride, long long o_batch_stride,
+                   long long lse_head_stride, long long lse_batch_stride, void* stream) {
+  if (B < 1 || H < 1 || rows < 0) return LCB_ERR_ARG;
+  if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
+  if (o_b_dtype != LCB_DTYPE_BF16 && o_b_dtype != LCB_DTYPE_F32) return LCB_ERR_UNSUPPORTED;
+  if (rows == 0) return LCB_OK;
+  if (!o_acc || !lse_acc || !o_b || !lse_b || !aligned16(o_acc) || !aligned16(o_b)) return LCB_ERR_ARG;
+  if (o_out_bf16 && !aligned16(o_out_bf16)) return LCB_ERR_ARG;
+  if (!stride_ok(o_row_stride) || !stride_ok(o_batch_stride) || o_row_stride < static_cast<long long>(H) * D)
+    return LCB_ERR_ARG;
+  if (lse_head_stride < 0 || lse_batch_stride < 0) return LCB_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return finish(launch_lse_merge(o_acc, lse_acc, o_b, o_b_dtype == LCB_DTYPE_F32, lse_b, o_out_bf16, B, H, rows,
+                                 o_row_stride, o_batch_stride, lse_head_stride, lse_batch_stride, st),
+                st);
+}
+
+int zigzag_schedule(int S, int P, int* perm, lcb_task* tasks) {
+  if (P < 1 || S < 2 * P || S % (2 * P) != 0) return LCB_ERR_SCHEDULE;
+  const int c = S / (2 * P);
+  if (perm) {
+    for (int r = 0; r < P; ++r) {
+      const int early = r, late = 2 * P - 1 - r;
+      for (int t = 0; t < c; ++t) {
+        perm[r * 2 * c + t] = early * c + t;
+        perm[r * 2 * c + c + t] = late * c + t;
+      }
+    }
+  }
+  if (tasks) {
+    for (int r = 0; r < P; ++r) {
+      for (int s = 0; s < P; ++s) {
+        const int src = ((r - s) % P + P) % P;
+        lcb_task t;
+        t.rank = r;
+        t.step = s;
+        t.src = src;
+        if (s == 0) {
+          t.kind = LCB_TASK_DIAG;
+          t.q_off = r * 2 * c;
+          t.q_len = 2 * c;
+          t.k_off = r * 2 * c;
+          t.k_len = 2 * c;
+          t.causal = 1;
+        } else if (src < r) {
+          t.kind = LCB_TASK_LOWER;
+          t.q_off = r * 2 * c;
+          t.q_len = 2 * c;
+          t.k_off = src * 2 * c;
+          t.k_len = c;
+          t.causal = 0;
+        } else {
+          t.kind = LCB_TASK_UPPER;
+          t.q_off = r * 2 * c + c;
+          t.q_len = c;
+          t.k_off = src * 2 * c;
+          t.k_len = 2 * c;
+          t.causal = 0;
+        }
+        tasks[r * P + s] = t;
+      }
+    }
+  }
+  return LCB_OK;
+}
+
+static int permute_common(const void* src, void* dst, const int* perm, int rows, long long row_bytes, int scatter,
+                          void* stream) {
+  if (rows < 0 || row_bytes <= 0 || (row_bytes % 16)) return LCB_ERR_ARG;
+  if (rows == 0) return LCB_OK;
+  if (!src || !dst || !perm || src == dst || !aligned16(src) || !aligned16(dst)) return LCB_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return finish(launch_permute_rows(src, dst, perm, rows, row_bytes, scatter, st), st);
+}
+
+int lcb_permute_rows(const void* src, void* dst, const int* perm, int rows, long long row_bytes, void* stream) {
+  return permute_common(src, dst, perm, rows, row_bytes, 0, stream);
+}
+
+int lcb_scatter_rows(const void* src, void* dst, const int* perm, int rows, long long row_bytes, void* stream) {
+  return permute_common(src, dst, perm, rows, row_bytes, 1, stream);
+}
+
+int lcb_cast_f32_bf16(const float* src, void* dst, long long n, void* stream) {
+  if (n < 0) return LCB_ERR_ARG;
+  if (n == 0) return LCB_OK;
+  if (!src || !dst || !aligned16(src) || !aligned16(dst)) return LCB_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return finish(launch_cast_f32_bf16(src, dst, n, st), st);
+}
+
+int lcb_selftest_bounded_wait(void* stream) {
+  DevStatus st;
+  int rc = dev_status(&st);
+  if (rc != LCB_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = launch_wait_selftest(st, s)) != LCB_OK) return rc;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LCB_ERR_CUDA;
+  uint32_t bits = 0;
+  if ((rc = take_status(&bits, nullptr)) != LCB_OK) return rc;
+  return (bits & DEV_TIMEOUT) ? LCB_ERR_TIMEOUT : LCB_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Host-side plumbing shared by the C-ABI layer and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace lcb {
+
+// A [B, rows, H, D] bf16/fp32 view: element (b, s, h, d) lives at
+// base + b * batch_stride + s * row_stride + h * D + d (strides in elements).
+struct RowView {
+  const void* ptr;
+  long long row_stride;
+  long long batch_stride;
+};
+
+// Builds a 3-D TMA map over a bf16 [B, rows, H*D] view with a box of
+// 64 (inner, 128 bytes) x box_rows x 1 and 128-byte swizzle.
+// Returns 0 on success, a negative LCB status on failure.
+int make_tma_map_bf16(CUtensorMap* map, const RowView& v, int B, int rows, int HD, int box_rows);
+
+struct FwdLaunch {
+  RowView q, k, v;
+  void* o;
+  float* lse;
+  long long o_row_stride, o_batch_stride;
+  long long lse_head_stride, lse_batch_stride;
+  int B, H, Sq, Sk, causal, o_f32;
+  float scale;
+  DevStatus st;
+};
+int launch_attn_fwd(const FwdLaunch& a, cudaStream_t stream);
+
+struct BwdLaunch {
+  RowView q, k, v, dO;
+  const float* lse;
+  const float* delta;
+  long long lse_head_stride, lse_batch_stride;  // also used for delta
+  void* dq;
+  void* dk;
+  void* dv;
+  long long dq_row_stride, dq_batch_stride;    // in elements of the gradient dtype
+  long long dkv_row_stride, dkv_batch_stride;
+  int B, H, Sq, Sk, causal, grad_mode;  // LCB_GRAD_*
+  float scale;
+  DevStatus st;
+};
+int launch_attn_bwd_dkdv(const BwdLaunch& a, cudaStream_t stream);
+int launch_attn_bwd_dq(const BwdLaunch& a, cudaStream_t stream);
+
+int launch_bwd_preprocess(const void* o, const void* dO, long long row_stride, long long batch_stride, float* delta,
+                          long long d_head_stride, long long d_batch_stride, int B, int H, int S, cudaStream_t stream);
+
+int launch_lse_merge(float* o_acc, float* lse_acc, const void* o_b, int o_b_f32, const float* lse_b, void* o_out_bf16,
+                     int B, int H, int rows, long long o_row_stride, long long o_batch_stride,
+                     long long lse_head_stride, long long lse_batch_stride, cudaStream_t stream);
+
+int launch_permute_rows(const void* src, void* dst, const int* perm, int rows, long long row_bytes, int scatter,
+                        cudaStream_t stream);
+
+int launch_fill_empty(void* o, int o_f32, long long o_row_stride, long long o_batch_stride, float* lse,
+                      long long lse_head_stride, long long lse_batch_stride, int B, int H, int rows,
+                      cudaStream_t stream);
+
+int launch_wait_selftest(DevStatus st, cudaStream_t stream);
+
+int launch_cast_f32_bf16(const float* src, void* dst, long long n, cudaStream_t stream);
+
+}  // namespace lcb

@@ -1,0 +1,111 @@
+"""Zigzag ring attention emulated on one GPU.
+
+Zigzag ring attention ("EasyContext代码解析200行核心训练脚本实现原理",
+§模型并行策略解析 zigzag_ring_attn; the per-rank split of §训练循环核心逻辑)
+gives each of P ranks two of the 2P sequence chunks, r and 2P-1-r, and moves
+keys/values around a ring for P steps. Ring steps compose by merging partial
+(O, LSE) results ("EasyContext核心技术解析：序列并行与Flash Attention的完美结合",
+§1 "序列并行技术").
+
+Here the P ranks are virtual: every rank's data lives in one device's memory in
+zigzag order (rank-major), a ring "transfer" is a pointer to the owner's rows,
+and no collective runs. Steps are executed step-major (all ranks' step 0, then
+step 1, ...), as the real ring would run them in parallel. Every piece of
+arithmetic runs in libattn.so kernels:
+
+  forward  step 0 (DIAG): attn_fwd_ex, causal, writing the fp32 accumulator
+           step s > 0   : attn_fwd_ex (non-causal block, bf16) then
+                          attn_lse_merge into the fp32 accumulator
+           end          : lcb_cast_f32_bf16 of the accumulator
+  backward Delta from the final bf16 O (attn_bwd_preprocess), then per task
+           attn_bwd_ex with the rank's FINAL merged LSE and Delta; fp32
+           gradients are stored at step 0 and accumulated after, dQ into the
+           querying rank's rows and dK/dV into the owning rank's rows; a cast
+           to bf16 ends it.
+
+Outputs stay in zigzag order, the layout each rank would hold.
+"""
+
+import torch
+
+from . import _lib
+
+
+class ZigzagPlan:
+    """Schedule of one (S, P) zigzag ring and the gather into zigzag order."""
+
+    def __init__(self, S, P, device):
+        perm, tasks = _lib.zigzag_schedule(S, P)
+        self.S, self.P = S, P
+        self.c = S // (2 * P)
+        self.perm = perm
+        self.tasks = tasks
+        self.perm_dev = torch.tensor(perm, dtype=torch.int32, device=device)
+        # step-major order: every rank's step s before any rank's step s + 1
+        self.order = sorted(tasks, key=lambda t: (t["step"], t["rank"]))
+
+    def gather(self, x):
+        """[1, S, H, D] natural order -> zigzag order (a new tensor)."""
+        out = torch.empty_like(x)
+        return _lib.permute_rows(x, out, self.perm_dev, scatter=False)
+
+    def scatter(self, x):
+        """zigzag order -> natural order (a new tensor)."""
+        out = torch.empty_like(x)
+        return _lib.permute_rows(x, out, self.perm_dev, scatter=True)
+
+
+def zigzag_attention_fwd(qz, kz, vz, plan, scale=None, o_acc=None, lse=None, o_blk=None, lse_blk=None, o=None):
+    """Forward of the emulated ring on zigzag-ordered [1, S, H, D] bf16 inputs.
+
+    Returns (o bf16, lse fp32 [1, H, S], o_acc fp32), all in zigzag order.
+    Buffers may be passed in to keep allocation out of a timed loop.
+    """
+    B, S, H, D = qz.shape
+    if B != 1 or S != plan.S:
+        raise ValueError("zigzag emulation takes B = 1 and the plan's S")
+    scale = D ** -0.5 if scale is None else scale
+    dev = qz.device
+    c2 = 2 * plan.c
+    o_acc = torch.empty((1, S, H, D), dtype=torch.float32, device=dev) if o_acc is None else o_acc
+    lse = torch.empty((1, H, S), dtype=torch.float32, device=dev) if lse is None else lse
+    o_blk = torch.empty((1, c2, H, D), dtype=torch.bfloat16, device=dev) if o_blk is None else o_blk
+    lse_blk = torch.empty((1, H, c2), dtype=torch.float32, device=dev) if lse_blk is None else lse_blk
+    o = torch.empty_like(qz) if o is None else o
+    for t in plan.order:
+        qs = slice(t["q_off"], t["q_off"] + t["q_len"])
+        ks = slice(t["k_off"], t["k_off"] + t["k_len"])
+        if t["step"] == 0:
+            _lib.attn_fwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], o_acc[:, qs], lse[:, :, qs], True, scale)
+        else:
+            n = t["q_len"]
+            _lib.attn_fwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], o_blk[:, :n], lse_blk[:, :, :n], False, scale)
+            _lib.attn_lse_merge(o_acc[:, qs], lse[:, :, qs], o_blk[:, :n], lse_blk[:, :, :n])
+    _lib.cast_f32_bf16(o_acc, o)
+    return o, lse, o_acc
+
+
+def zigzag_attention_bwd(qz, kz, vz, oz, lse, doz, plan, scale=None, delta=None, grads32=None, grads=None):
+    """Backward of the emulated ring; all tensors in zigzag order.
+
+    Returns (dq, dk, dv) bf16 [1, S, H, D].
+    """
+    B, S, H, D = qz.shape
+    scale = D ** -0.5 if scale is None else scale
+    dev = qz.device
+    delta = torch.empty((1, H, S), dtype=torch.float32, device=dev) if delta is None else delta
+    if grads32 is None:
+        grads32 = tuple(torch.empty((1, S, H, D), dtype=torch.float32, device=dev) for _ in range(3))
+    if grads is None:
+        grads = tuple(torch.empty_like(qz) for _ in range(3))
+    dq32, dk32, dv32 = grads32
+    _lib.attn_bwd_preprocess(oz, doz, delta)
+    for t in plan.order:
+        qs = slice(t["q_off"], t["q_off"] + t["q_len"])
+        ks = slice(t["k_off"], t["k_off"] + t["k_len"])
+        _lib.attn_bwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], lse[:, :, qs], delta[:, :, qs], doz[:, qs],
+                         dq32[:, qs], dk32[:, ks], dv32[:, ks], bool(t["causal"]), scale,
+                         accumulate=t["step"] > 0)
+    for g32, g in zip(grads32, grads):
+        _lib.cast_f32_bf16(g32, g)
+    return grads
