@@ -1,0 +1,363 @@
+#!/usr/bin/env python3
+"""Causal attention fwd+bwd throughput on GB300.
+
+Workload: one Llama-2-7B attention layer, B=1, H=32, S=32768, D=128, causal,
+bf16 Q/K/V/dO drawn i.i.d. N(0,1) from a seed (synthetic, no dataset), scale
+1/sqrt(128). A step is the whole hot path once: attn_fwd, the Delta
+preprocess, the dK/dV pass and the dQ pass (all libattn.so kernels).
+
+FLOP convention (causal, half of the S x S pairs): forward 2*B*H*S^2*D,
+backward 2.5 x forward, step 7*B*H*S^2*D.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own layer (the
+path shards by independent problems, no collective); value is the whole
+job's FLOP / the slowest rank's time. One JSON line is printed by rank 0.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal attn fwd+bwd TFLOP/s and % of GB300 BF16 peak at S=32K–512K, H=32, D=128"
+UNIT = "TFLOP/s"
+B, H, S, D = 1, 32, 32768, 128
+WORKLOAD = "llama2-7b-attention-layer causal fwd+bwd B1 H32 S32768 D128"
+L2_NOTE = "inputs larger than L2: q,k,v,dO are 268 MB each (1.07 GB per step) vs 129 MB L2; no flush"
+# Oracle sample for the CPU legs: head 0, the causal prefix of this many tokens (fwd+bwd).
+CPU_SAMPLE_S = 8192
+
+
+def step_flop(b, h, s, d):
+    return 7.0 * b * h * s * s * d
+
+
+def fwd_flop(b, h, s, d):
+    return 2.0 * b * h * s * s * d
+
+
+def load_peaks():
+    """(tensor TFLOP/s sustained, tensor burst, HBM GB/s, source)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        burst = float(pk.get("bf16_tflops"))
+        sus = float(pk.get("bf16_tflops_sustained", burst))
+        hbm = float(pk.get("hbm_gbs"))
+        return sus, burst, hbm, "measured"
+    except Exception:
+        return 1700.0, 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_median": statistics.median(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def cpu_oracle_sample(q, k, v, do, s_sample):
+    """Times the fp64 oracle (fwd + bwd by the definition) on head 0's causal prefix."""
+    import numpy as np
+
+    import oracle
+
+    f64 = lambda t: t[:, :s_sample, :1].float().cpu().numpy().astype(np.float64)  # noqa: E731
+    qs, ks, vs, dos = f64(q), f64(k), f64(v), f64(do)
+    t0 = time.perf_counter()
+    oracle.attn_bwd(qs, ks, vs, dos, True, D ** -0.5)
+    dt = time.perf_counter() - t0
+    return dt, step_flop(1, 1, s_sample, D)
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands on the host cores, same metric and unit."""
+    if rank != 0:
+        return 0
+    import torch
+
+    from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo
+
+    q, k, v, do = gaussian_qkvdo(1, 1, CPU_SAMPLE_S, D, seed=0, device="cpu")
+    times = []
+    flop = None
+    for i in range(args.warmup + args.steps):
+        dt, flop = cpu_oracle_sample(q, k, v, do, CPU_SAMPLE_S)
+        if i >= args.warmup:
+            times.append(dt)
+    t = sum(times)
+    value = flop * len(times) / t / 1e12
+    cores = os.cpu_count()
+    sample = f"fp64 oracle fwd+bwd of one head's causal prefix of {CPU_SAMPLE_S} tokens (H=1 of 32, S={CPU_SAMPLE_S} of {S})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "S": S, "D": D, "causal": True,
+                   "global_batch": 1, "seq_len": S, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import long_context_causal_blockwise_gb300 as lcb
+    from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lcb.load()
+    scale = D ** -0.5
+    q, k, v, do = gaussian_qkvdo(B, H, S, D, seed=rank, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, S, device=dev)
+    delta = torch.empty(B, H, S, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+
+    names = ("attn_fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        lcb.attn_fwd(q, k, v, causal=True, scale=scale, o=o, lse=lse)
+        if evs is not None:
+            evs[1].record(stream)
+        lcb.attn_bwd_preprocess(o, do, delta)
+        if evs is not None:
+            evs[2].record(stream)
+        lcb.attn_bwd_ex(q, k, v, lse, delta, do, dq, dk, dv, True, scale, passes="dkdv")
+        if evs is not None:
+            evs[3].record(stream)
+        lcb.attn_bwd_ex(q, k, v, lse, delta, do, dq, dk, dv, True, scale, passes="dq")
+        if evs is not None:
+            evs[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)  # let the sampler attach before the timed work
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(events[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    t_max = elapsed
+    if world > 1:
+        tt = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    per = {n: [] for n in names}
+    for evs in events:
+        for j, n in enumerate(names):
+            per[n].append(evs[j].elapsed_time(evs[j + 1]) / 1e3)
+    avg = {n: sum(v_) / len(v_) for n, v_ in per.items()}
+
+    # ---------------- end to end through the public calls, host buffers in and out
+    e2e_steps = max(1, min(args.steps, 5))
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
+    hq, hk, hv, hdo = (pin(t) for t in (q, k, v, do))
+    for h_, d_ in ((hq, q), (hk, k), (hv, v), (hdo, do)):
+        h_.copy_(d_)
+    ho, hlse, hdq, hdk, hdv = pin(o), pin(lse), pin(dq), pin(dk), pin(dv)
+    ws = torch.empty(lcb.attn_bwd_workspace_bytes(B, H, S, D), dtype=torch.uint8, device=dev)
+    dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    q_, k_, v_, do_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(do)
+    o_, lse_ = torch.empty_like(o), torch.empty_like(lse)
+
+    def e2e_step():
+        for d_, h_ in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo)):
+            d_.copy_(h_, non_blocking=True)
+        lcb.attn_fwd(q_, k_, v_, causal=True, scale=scale, o=o_, lse=lse_)
+        lcb.attn_bwd(q_, k_, v_, o_, lse_, do_, causal=True, scale=scale, dq=dq_, dk=dk_, dv=dv_, workspace=ws)
+        for h_, d_ in ((ho, o_), (hlse, lse_), (hdq, dq_), (hdk, dk_), (hdv, dv_)):
+            h_.copy_(d_, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_t = e0.elapsed_time(e1) / 1e3 / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_t], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_t = float(tt.item())
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v, do))
+    d2h = sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv))
+    # the e2e outputs must equal the device-resident run's
+    same = bool(torch.equal(ho.to(dev), o) and torch.equal(hdq.to(dev), dq))
+
+    if rank != 0:
+        return 0
+
+    sus, burst, hbm, src = load_peaks()
+    flop = step_flop(B, H, S, D)
+    value = world * flop * args.steps / t_max / 1e12
+    ms = 1e3 * t_max / args.steps
+    pairs = B * H * S * S / 2.0  # causal (query, key) pairs, the R5 convention
+    alg = {  # algorithmic work per launch
+        "attn_fwd": ("tensor", 4 * D * pairs),            # S = QK^T and O += PV
+        "bwd_dkdv": ("tensor", 8 * D * pairs),            # S^T, dP^T, dV, dK
+        "bwd_dq": ("tensor", 6 * D * pairs),              # S, dP, dQ
+        "bwd_preprocess": ("hbm", 2 * B * S * H * D * 2 + B * S * H * 4),
+    }
+    kernels = {}
+    for n in names:
+        kind, work = alg[n]
+        t = avg[n]
+        if kind == "tensor":
+            ach = work / t / 1e12
+            kernels[n] = {"ms": 1e3 * t, "tflops": ach, "frac_of_peak": ach / sus}
+        else:
+            ach = work / t / 1e9
+            kernels[n] = {"ms": 1e3 * t, "gbs": ach, "frac_of_peak": ach / hbm}
+    dom = max(("attn_fwd", "bwd_dkdv", "bwd_dq", "bwd_preprocess"), key=lambda n: avg[n])
+    kind, work = alg[dom]
+    if kind == "tensor":
+        ach = work / avg[dom] / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": sus, "unit": "TFLOP/s", "frac": ach / sus,
+                "traffic": None, "peak_source": f"{src} bf16 sustained"}
+    else:
+        ach = work / avg[dom] / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": None, "peak_source": f"{src} HBM copy"}
+    fwd_t = avg["attn_fwd"]
+    bwd_t = avg["bwd_preprocess"] + avg["bwd_dkdv"] + avg["bwd_dq"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "S": S, "D": D, "causal": True, "l2": L2_NOTE,
+                   "global_batch": world, "seq_len": S, "parallelism": f"dp{world} (one independent layer per GPU)"},
+        "pct_of_peak": 100.0 * (value / world) / sus,
+        "peak_tflops": sus, "peak_source": f"{src} bf16 sustained",
+        "fwd_tflops": fwd_flop(B, H, S, D) / fwd_t / 1e12,
+        "bwd_tflops": 2.5 * fwd_flop(B, H, S, D) / bwd_t / 1e12,
+        "fwd_frac_of_peak": fwd_flop(B, H, S, D) / fwd_t / 1e12 / sus,
+        "bwd_frac_of_peak": 2.5 * fwd_flop(B, H, S, D) / bwd_t / 1e12 / sus,
+        "kernels": kernels,
+        "roofline": roof,
+        "e2e": {"value": world * flop / e2e_t / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_t, "matches_device_run": same},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        dt, cflop = cpu_oracle_sample(q, k, v, do, CPU_SAMPLE_S)
+        line["cpu_baseline"] = {
+            "value": cflop / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd of head 0's causal prefix of {CPU_SAMPLE_S} tokens, {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -150,6 +150,25 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const float* lse, c
                 long long dkv_batch_stride, void* stream);
 
 /*
+ * attn_bwd_dkdv_ex / attn_bwd_dq_ex — the two passes of attn_bwd_ex on their
+ * own, same arguments and semantics: the first writes only dk and dv (dq is
+ * not touched), the second only dq (dk, dv not touched). Given Delta, the two
+ * passes are independent and may run on different streams.
+ */
+int attn_bwd_dkdv_ex(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                     const void* dO, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, int causal,
+                     float scale, long long q_row_stride, long long q_batch_stride, long long kv_row_stride,
+                     long long kv_batch_stride, long long lse_head_stride, long long lse_batch_stride,
+                     int grad_mode, long long dq_row_stride, long long dq_batch_stride, long long dkv_row_stride,
+                     long long dkv_batch_stride, void* stream);
+int attn_bwd_dq_ex(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, int causal,
+                   float scale, long long q_row_stride, long long q_batch_stride, long long kv_row_stride,
+                   long long kv_batch_stride, long long lse_head_stride, long long lse_batch_stride, int grad_mode,
+                   long long dq_row_stride, long long dq_batch_stride, long long dkv_row_stride,
+                   long long dkv_batch_stride, void* stream);
+
+/*
  * attn_lse_merge — fold a partial result into an accumulator, [SP]:
  *   m = max(L_acc, L_b), w_x = exp(L_x - m),
  *   L_acc <- m + ln(w_acc + w_b),  O_acc <- (w_acc O_acc + w_b O_b)/(w_acc + w_b)

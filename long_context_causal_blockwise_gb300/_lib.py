@@ -54,6 +54,10 @@ _SIGNATURES = {
     "attn_bwd_preprocess": ([_P, _P, _P, _I, _I, _I, _I, _LL, _LL, _LL, _LL, _P], _I),
     "attn_bwd_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _I,
                      _LL, _LL, _LL, _LL, _P], _I),
+    "attn_bwd_dkdv_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL,
+                          _I, _LL, _LL, _LL, _LL, _P], _I),
+    "attn_bwd_dq_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _I,
+                        _LL, _LL, _LL, _LL, _P], _I),
     "attn_lse_merge": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _LL, _LL, _LL, _LL, _P], _I),
     "zigzag_schedule": ([_I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(LcbTask)], _I),
     "lcb_permute_rows": ([_P, _P, _P, _I, _LL, _P], _I),
@@ -205,7 +209,7 @@ def attn_bwd_preprocess(o, do, delta):
     return delta
 
 
-def attn_bwd_ex(q, k, v, lse, delta, do, dq, dk, dv, causal, scale, accumulate=True):
+def attn_bwd_ex(q, k, v, lse, delta, do, dq, dk, dv, causal, scale, accumulate=True, passes="both"):
     """Block backward with given row statistics.
 
     bf16 gradients are overwritten; fp32 gradients are accumulated into
@@ -232,7 +236,8 @@ def attn_bwd_ex(q, k, v, lse, delta, do, dq, dk, dv, causal, scale, accumulate=T
     dkr, dkb = _bshd(dk, "dk", gdt)
     if _bshd(dv, "dv", gdt) != (dkr, dkb):
         raise ValueError("dk and dv must share strides")
-    _check("attn_bwd_ex", load().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(do), _ptr(dq),
+    fname = {"both": "attn_bwd_ex", "dkdv": "attn_bwd_dkdv_ex", "dq": "attn_bwd_dq_ex"}[passes]
+    _check(fname, getattr(load(), fname)(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(do), _ptr(dq),
                                              _ptr(dk), _ptr(dv), B, H, Sq, Sk, D, int(causal), float(scale), qr, qb,
                                              kr, kb, lh, lb, grad_mode, dqr, dqb, dkr, dkb, _stream(q)))
     return dq, dk, dv

@@ -237,12 +237,13 @@ int attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int 
                 st);
 }
 
-int attn_bwd_ex(const void* q, const void* k, const void* v, const float* lse, const float* delta,
-                const void* dO, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, int causal,
-                float scale, long long q_row_stride, long long q_batch_stride, long long kv_row_stride,
-                long long kv_batch_stride, long long lse_head_stride, long long lse_batch_stride, int grad_mode,
-                long long dq_row_stride, long long dq_batch_stride, long long dkv_row_stride,
-                long long dkv_batch_stride, void* stream) {
+// Validates the arguments shared by the block-backward entry points and fills `a`.
+static int prep_bwd(BwdLaunch* a, const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, int causal,
+                    float scale, long long q_row_stride, long long q_batch_stride, long long kv_row_stride,
+                    long long kv_batch_stride, long long lse_head_stride, long long lse_batch_stride, int grad_mode,
+                    long long dq_row_stride, long long dq_batch_stride, long long dkv_row_stride,
+                    long long dkv_batch_stride) {
   if (B < 1 || H < 1 || Sq < 0 || Sk < 0) return LCB_ERR_ARG;
   if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
   if (causal != 0 && causal != 1) return LCB_ERR_ARG;
@@ -250,7 +251,6 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const float* lse, c
   if (grad_mode != LCB_GRAD_BF16 && grad_mode != LCB_GRAD_F32_ACCUM && grad_mode != LCB_GRAD_F32_STORE)
     return LCB_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !std::isfinite(scale)) return LCB_ERR_ARG;
-  if (Sq == 0 && Sk == 0) return LCB_OK;
   if (!q || !k || !v || !lse || !delta || !dO || !dq || !dk || !dv) return LCB_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) ||
       !aligned16(dv))
@@ -262,38 +262,74 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const float* lse, c
   const long long HD = static_cast<long long>(H) * kHeadDim;
   if (HD > q_row_stride || HD > kv_row_stride || HD > dq_row_stride || HD > dkv_row_stride) return LCB_ERR_ARG;
   if (lse_head_stride < 0 || lse_batch_stride < 0) return LCB_ERR_ARG;
+  a->q = {q, q_row_stride, q_batch_stride};
+  a->dO = {dO, q_row_stride, q_batch_stride};
+  a->k = {k, kv_row_stride, kv_batch_stride};
+  a->v = {v, kv_row_stride, kv_batch_stride};
+  a->lse = lse;
+  a->delta = delta;
+  a->lse_head_stride = lse_head_stride;
+  a->lse_batch_stride = lse_batch_stride;
+  a->dq = dq;
+  a->dk = dk;
+  a->dv = dv;
+  a->dq_row_stride = dq_row_stride;
+  a->dq_batch_stride = dq_batch_stride;
+  a->dkv_row_stride = dkv_row_stride;
+  a->dkv_batch_stride = dkv_batch_stride;
+  a->B = B;
+  a->H = H;
+  a->Sq = Sq;
+  a->Sk = Sk;
+  a->causal = causal;
+  a->grad_mode = grad_mode;
+  a->scale = scale;
+  return dev_status(&a->st);
+}
+
+#define LCB_BWD_EX_ARGS                                                                                           \
+  q, k, v, lse, delta, dO, dq, dk, dv, B, H, Sq, Sk, D, causal, scale, q_row_stride, q_batch_stride, kv_row_stride, \
+      kv_batch_stride, lse_head_stride, lse_batch_stride, grad_mode, dq_row_stride, dq_batch_stride, dkv_row_stride,   \
+      dkv_batch_stride
+
+int attn_bwd_dkdv_ex(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                     const void* dO, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, int causal,
+                     float scale, long long q_row_stride, long long q_batch_stride, long long kv_row_stride,
+                     long long kv_batch_stride, long long lse_head_stride, long long lse_batch_stride,
+                     int grad_mode, long long dq_row_stride, long long dq_batch_stride, long long dkv_row_stride,
+                     long long dkv_batch_stride, void* stream) {
   BwdLaunch a;
-  a.q = {q, q_row_stride, q_batch_stride};
-  a.dO = {dO, q_row_stride, q_batch_stride};
-  a.k = {k, kv_row_stride, kv_batch_stride};
-  a.v = {v, kv_row_stride, kv_batch_stride};
-  a.lse = lse;
-  a.delta = delta;
-  a.lse_head_stride = lse_head_stride;
-  a.lse_batch_stride = lse_batch_stride;
-  a.dq = dq;
-  a.dk = dk;
-  a.dv = dv;
-  a.dq_row_stride = dq_row_stride;
-  a.dq_batch_stride = dq_batch_stride;
-  a.dkv_row_stride = dkv_row_stride;
-  a.dkv_batch_stride = dkv_batch_stride;
-  a.B = B;
-  a.H = H;
-  a.Sq = Sq;
-  a.Sk = Sk;
-  a.causal = causal;
-  a.grad_mode = grad_mode;
-  a.scale = scale;
-  int rc = dev_status(&a.st);
+  int rc = prep_bwd(&a, LCB_BWD_EX_ARGS);
   if (rc != LCB_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (Sk > 0) {
-    if ((rc = launch_attn_bwd_dkdv(a, st)) != LCB_OK) return rc;
-  }
-  if (Sq > 0) {
-    if ((rc = launch_attn_bwd_dq(a, st)) != LCB_OK) return rc;
-  }
+  return finish(launch_attn_bwd_dkdv(a, st), st);
+}
+
+int attn_bwd_dq_ex(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, int causal,
+                   float scale, long long q_row_stride, long long q_batch_stride, long long kv_row_stride,
+                   long long kv_batch_stride, long long lse_head_stride, long long lse_batch_stride, int grad_mode,
+                   long long dq_row_stride, long long dq_batch_stride, long long dkv_row_stride,
+                   long long dkv_batch_stride, void* stream) {
+  BwdLaunch a;
+  int rc = prep_bwd(&a, LCB_BWD_EX_ARGS);
+  if (rc != LCB_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return finish(launch_attn_bwd_dq(a, st), st);
+}
+
+int attn_bwd_ex(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                const void* dO, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, int causal,
+                float scale, long long q_row_stride, long long q_batch_stride, long long kv_row_stride,
+                long long kv_batch_stride, long long lse_head_stride, long long lse_batch_stride, int grad_mode,
+                long long dq_row_stride, long long dq_batch_stride, long long dkv_row_stride,
+                long long dkv_batch_stride, void* stream) {
+  BwdLaunch a;
+  int rc = prep_bwd(&a, LCB_BWD_EX_ARGS);
+  if (rc != LCB_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((rc = launch_attn_bwd_dkdv(a, st)) != LCB_OK) return rc;
+  if ((rc = launch_attn_bwd_dq(a, st)) != LCB_OK) return rc;
   return finish(LCB_OK, st);
 }
 

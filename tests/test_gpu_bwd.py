@@ -1,0 +1,124 @@
+"""GPU parity of the backward passes (dK/dV and dQ) against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import long_context_causal_blockwise_gb300 as lcb
+from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo, sample_rows
+from parity import assert_bf16_close, to64
+
+pytestmark = pytest.mark.gpu
+D = 128
+
+
+def _bwd_full_check(B, H, S, causal, seed):
+    q, k, v, do = gaussian_qkvdo(B, H, S, D, seed=seed)
+    o, lse = lcb.attn_fwd(q, k, v, causal=causal)
+    dq, dk, dv = lcb.attn_bwd(q, k, v, o, lse, do, causal=causal)
+    torch.cuda.synchronize()
+    ref = oracle.attn_bwd(to64(q), to64(k), to64(v), to64(do), causal, D ** -0.5)
+    tag = f"B{B} H{H} S{S} causal{causal}"
+    assert_bf16_close(to64(dq), ref["dq"], "dQ " + tag)
+    assert_bf16_close(to64(dk), ref["dk"], "dK " + tag)
+    assert_bf16_close(to64(dv), ref["dv"], "dV " + tag)
+
+
+def test_config1_shape_backward_full_tensors():
+    _bwd_full_check(1, 4, 1024, True, seed=0)
+
+
+@pytest.mark.parametrize("S", [1, 7, 128, 129, 256, 383, 1000])
+@pytest.mark.parametrize("causal", [True, False])
+def test_ragged_lengths(S, causal):
+    _bwd_full_check(2, 2, S, causal, seed=100 + S)
+
+
+def test_block_backward_accumulates_to_monolithic():
+    """Key blocks with the full problem's LSE/Delta, fp32 accumulate, add up exactly."""
+    B, H, Sq, Sk = 1, 2, 256, 640
+    g = torch.Generator(device="cuda").manual_seed(3)
+    mk = lambda n: torch.randn(B, n, H, D, generator=g, device="cuda").to(torch.bfloat16)  # noqa: E731
+    q, k, v, do = mk(Sq), mk(Sk), mk(Sk), mk(Sq)
+    o = torch.empty(B, Sq, H, D, device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty(B, H, Sq, device="cuda")
+    lcb.attn_fwd_ex(q, k, v, o, lse, False, D ** -0.5)
+    delta = torch.empty(B, H, Sq, device="cuda")
+    lcb.attn_bwd_preprocess(o, do, delta)
+    dq = torch.empty(B, Sq, H, D, device="cuda")
+    dk = torch.empty(B, Sk, H, D, device="cuda")
+    dv = torch.empty(B, Sk, H, D, device="cuda")
+    cuts = [(0, 200), (200, 456), (456, 640)]
+    for n, (a, b) in enumerate(cuts):
+        # dq accumulates over blocks; each block's dk/dv rows are stored once
+        lcb.attn_bwd_ex(q, k[:, a:b], v[:, a:b], lse, delta, do, dq, dk[:, a:b], dv[:, a:b], False, D ** -0.5,
+                        accumulate=n > 0)
+    torch.cuda.synchronize()
+    ref = oracle.attn_bwd(to64(q), to64(k), to64(v), to64(do), False, D ** -0.5)
+    assert_bf16_close(to64(dq), ref["dq"], "dQ blocks", max_abs=5e-3, mean_abs=5e-4)
+    assert_bf16_close(to64(dk), ref["dk"], "dK blocks", max_abs=5e-3, mean_abs=5e-4)
+    assert_bf16_close(to64(dv), ref["dv"], "dV blocks", max_abs=5e-3, mean_abs=5e-4)
+
+
+def test_split_passes_match_combined():
+    B, H, S = 1, 2, 512
+    q, k, v, do = gaussian_qkvdo(B, H, S, D, seed=8)
+    o, lse = lcb.attn_fwd(q, k, v)
+    delta = torch.empty(B, H, S, device="cuda")
+    lcb.attn_bwd_preprocess(o, do, delta)
+    g1 = [torch.empty_like(q) for _ in range(3)]
+    g2 = [torch.full_like(q, 3.0) for _ in range(3)]
+    lcb.attn_bwd_ex(q, k, v, lse, delta, do, *g1, True, D ** -0.5)
+    lcb.attn_bwd_ex(q, k, v, lse, delta, do, *g2, True, D ** -0.5, passes="dkdv")
+    torch.cuda.synchronize()
+    assert torch.equal(g2[1], g1[1]) and torch.equal(g2[2], g1[2])
+    assert (g2[0] == 3.0).all()  # dq untouched by the dK/dV pass
+    lcb.attn_bwd_ex(q, k, v, lse, delta, do, *g2, True, D ** -0.5, passes="dq")
+    torch.cuda.synchronize()
+    assert torch.equal(g2[0], g1[0])
+
+
+def test_empty_sides():
+    """Sk = 0: dQ is zero; Sq = 0: dK and dV are zero."""
+    B, H = 1, 2
+    q = torch.randn(B, 64, H, D, device="cuda").to(torch.bfloat16)
+    e = torch.empty(B, 0, H, D, device="cuda", dtype=torch.bfloat16)
+    lse = torch.zeros(B, H, 64, device="cuda")
+    delta = torch.zeros(B, H, 64, device="cuda")
+    dq = torch.full_like(q, 5.0)
+    lcb.attn_bwd_ex(q, e, e, lse, delta, q, dq, e, e, False, D ** -0.5)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dq) == 0
+    dk = torch.full_like(q, 5.0)
+    dv = torch.full_like(q, 5.0)
+    le = torch.zeros(B, H, 0, device="cuda")
+    lcb.attn_bwd_ex(e, q, q, le, le, e, e, dk, dv, False, D ** -0.5)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
+
+
+def test_config2_sampled_rows_backward():
+    """B=1, H=32, S=32768: dQ on sampled query rows of every head; dK/dV on
+    sampled key rows of two heads; the sum invariants on every head."""
+    B, H, S = 1, 32, 32768
+    q, k, v, do = gaussian_qkvdo(B, H, S, D, seed=0)
+    o, lse = lcb.attn_fwd(q, k, v)
+    dq, dk, dv = lcb.attn_bwd(q, k, v, o, lse, do)
+    torch.cuda.synchronize()
+    rows = sample_rows(S, 128, seed=1)
+    q64, k64, v64, do64 = to64(q), to64(k), to64(v), to64(do)
+    ref = oracle.attn_rows(q64, k64, v64, do64, rows, True, D ** -0.5)
+    assert_bf16_close(to64(dq[:, rows]), ref["dq"], "dQ C2 sampled")
+    keys = sample_rows(S, 128, seed=2)
+    heads = [0, 31]
+    rdk, rdv = oracle.attn_key_rows(q64, k64, v64, do64, keys, heads, True, D ** -0.5)
+    assert_bf16_close(to64(dk[:, keys][:, :, heads]), rdk, "dK C2 sampled")
+    assert_bf16_close(to64(dv[:, keys][:, :, heads]), rdv, "dV C2 sampled")
+    # sum_j dV_j = sum_i dO_i and sum_j dK_j = 0, per head (fp32 sums of bf16 values)
+    sdv = dv.float().sum(1)
+    sdo = do.float().sum(1)
+    sdk = dk.float().sum(1)
+    tol = 1e-2 * sdo.norm(dim=-1, keepdim=True)
+    assert ((sdv - sdo).norm(dim=-1, keepdim=True) <= tol).all()
+    assert (sdk.norm(dim=-1) <= 1e-2 * dk.float().norm(dim=(1, 3))).all()
