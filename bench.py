@@ -38,6 +38,14 @@ L2_NOTE = "inputs larger than L2: q,k,v,dO are 268 MB each (1.07 GB per step) vs
 CPU_SAMPLE_S = 8192
 
 
+def _set_shape(h, s):
+    """Overrides the workload shape (used for small ncu captures, never for the bench line)."""
+    global H, S, WORKLOAD, L2_NOTE
+    H, S = h, s
+    WORKLOAD = f"causal fwd+bwd B1 H{h} S{s} D128 (profiling case)"
+    L2_NOTE = f"q,k,v,dO are {s * h * D * 2 / 1e6:.0f} MB each"
+
+
 def step_flop(b, h, s, d):
     return 7.0 * b * h * s * s * d
 
@@ -338,7 +346,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--H", type=int, default=H, help="heads (profiling of smaller cases only)")
+    ap.add_argument("--S", type=int, default=S, help="sequence length (profiling of smaller cases only)")
     args = ap.parse_args()
+    if (args.H, args.S) != (H, S):
+        _set_shape(args.H, args.S)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -172,15 +172,18 @@ int attn_bwd_dq_ex(const void* q, const void* k, const void* v, const float* lse
  * attn_lse_merge — fold a partial result into an accumulator, [SP]:
  *   m = max(L_acc, L_b), w_x = exp(L_x - m),
  *   L_acc <- m + ln(w_acc + w_b),  O_acc <- (w_acc O_acc + w_b O_b)/(w_acc + w_b)
- * Both sides -inf gives L = -inf, O = 0. o_acc fp32 and o_b (bf16 or fp32 per
- * o_b_dtype) are [B, rows, H, D] views with the same strides (elements);
- * lse_acc and lse_b are fp32 [B, H, rows] views with the same strides.
- * If o_out_bf16 is not NULL the merged O is also written there as bf16 (same
- * strides), which ends a ring without a separate cast.
+ * Both sides -inf gives L = -inf, O = 0. o_acc (fp32) and o_b (bf16 or fp32
+ * per o_b_dtype) are [B, rows, H, D] views, each with its own row/batch
+ * strides (elements); lse_acc and lse_b are fp32 [B, H, rows] views with
+ * their own head/batch strides. If o_out_bf16 is not NULL the merged O is
+ * also written there as bf16 with o_acc's strides, which ends a ring without
+ * a separate cast. In-place on (o_acc, lse_acc); o_b and lse_b are read only.
  */
 int attn_lse_merge(float* o_acc, float* lse_acc, const void* o_b, const float* lse_b, int o_b_dtype,
                    void* o_out_bf16, int B, int H, int rows, int D, long long o_row_stride, long long o_batch_stride,
-                   long long lse_head_stride, long long lse_batch_stride, void* stream);
+                   long long ob_row_stride, long long ob_batch_stride, long long lse_head_stride,
+                   long long lse_batch_stride, long long lseb_head_stride, long long lseb_batch_stride,
+                   void* stream);
 
 /*
  * zigzag_schedule — the zigzag split and ring task table, [ZZ]. HOST memory.

@@ -58,7 +58,7 @@ _SIGNATURES = {
                           _I, _LL, _LL, _LL, _LL, _P], _I),
     "attn_bwd_dq_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _I,
                         _LL, _LL, _LL, _LL, _P], _I),
-    "attn_lse_merge": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _LL, _LL, _LL, _LL, _P], _I),
+    "attn_lse_merge": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _LL, _LL, _LL, _LL, _LL, _LL, _LL, _LL, _P], _I),
     "zigzag_schedule": ([_I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(LcbTask)], _I),
     "lcb_permute_rows": ([_P, _P, _P, _I, _LL, _P], _I),
     "lcb_scatter_rows": ([_P, _P, _P, _I, _LL, _P], _I),
@@ -246,20 +246,20 @@ def attn_bwd_ex(q, k, v, lse, delta, do, dq, dk, dv, causal, scale, accumulate=T
 # ------------------------------------------------------------------ merge / zigzag
 
 def attn_lse_merge(o_acc, lse_acc, o_b, lse_b, o_out_bf16=None):
-    """In-place (o_acc fp32, lse_acc) <- merge with (o_b, lse_b)."""
+    """In-place (o_acc fp32, lse_acc) <- merge with (o_b bf16/fp32, lse_b)."""
     B, R, H, D = o_acc.shape
+    if o_b.shape != o_acc.shape or lse_b.shape != lse_acc.shape:
+        raise ValueError("merge operands must have matching shapes")
     r, b = _bshd(o_acc, "o_acc", torch.float32)
-    if _bshd(o_b, "o_b", o_b.dtype) != (r, b):
-        raise ValueError("o_acc and o_b must share strides")
+    rb, bb = _bshd(o_b, "o_b", o_b.dtype)
     lh, lb = _bhs(lse_acc, "lse_acc")
-    if _bhs(lse_b, "lse_b") != (lh, lb):
-        raise ValueError("lse_acc and lse_b must share strides")
+    lbh, lbb = _bhs(lse_b, "lse_b")
     if o_out_bf16 is not None and _bshd(o_out_bf16, "o_out_bf16") != (r, b):
         raise ValueError("o_out_bf16 must share o_acc's strides")
     odt = LCB_DTYPE_F32 if o_b.dtype == torch.float32 else LCB_DTYPE_BF16
     _check("attn_lse_merge", load().attn_lse_merge(_ptr(o_acc), _ptr(lse_acc), _ptr(o_b), _ptr(lse_b), odt,
                                                    None if o_out_bf16 is None else _ptr(o_out_bf16), B, H, R, D, r,
-                                                   b, lh, lb, _stream(o_acc)))
+                                                   b, rb, bb, lh, lb, lbh, lbb, _stream(o_acc)))
     return o_acc, lse_acc
 
 

@@ -251,7 +251,9 @@ static int prep_bwd(BwdLaunch* a, const void* q, const void* k, const void* v, c
   if (grad_mode != LCB_GRAD_BF16 && grad_mode != LCB_GRAD_F32_ACCUM && grad_mode != LCB_GRAD_F32_STORE)
     return LCB_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !std::isfinite(scale)) return LCB_ERR_ARG;
-  if (!q || !k || !v || !lse || !delta || !dO || !dq || !dk || !dv) return LCB_ERR_ARG;
+  // Operands of an empty side (Sq == 0: q, dO, lse, delta, dq; Sk == 0: k, v, dk, dv) may be NULL.
+  if (Sq > 0 && (!q || !lse || !delta || !dO || !dq)) return LCB_ERR_ARG;
+  if (Sk > 0 && (!k || !v || !dk || !dv)) return LCB_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) ||
       !aligned16(dv))
     return LCB_ERR_ARG;
@@ -351,19 +353,24 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
 
 int attn_lse_merge(float* o_acc, float* lse_acc, const void* o_b, const float* lse_b, int o_b_dtype,
                    void* o_out_bf16, int B, int H, int rows, int D, long long o_row_stride, long long o_batch_stride,
-                   long long lse_head_stride, long long lse_batch_stride, void* stream) {
+                   long long ob_row_stride, long long ob_batch_stride, long long lse_head_stride,
+                   long long lse_batch_stride, long long lseb_head_stride, long long lseb_batch_stride,
+                   void* stream) {
   if (B < 1 || H < 1 || rows < 0) return LCB_ERR_ARG;
   if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
   if (o_b_dtype != LCB_DTYPE_BF16 && o_b_dtype != LCB_DTYPE_F32) return LCB_ERR_UNSUPPORTED;
   if (rows == 0) return LCB_OK;
   if (!o_acc || !lse_acc || !o_b || !lse_b || !aligned16(o_acc) || !aligned16(o_b)) return LCB_ERR_ARG;
   if (o_out_bf16 && !aligned16(o_out_bf16)) return LCB_ERR_ARG;
-  if (!stride_ok(o_row_stride) || !stride_ok(o_batch_stride) || o_row_stride < static_cast<long long>(H) * D)
+  const long long HD = static_cast<long long>(H) * D;
+  if (!stride_ok(o_row_stride) || !stride_ok(o_batch_stride) || o_row_stride < HD) return LCB_ERR_ARG;
+  if (!stride_ok(ob_row_stride) || !stride_ok(ob_batch_stride) || ob_row_stride < HD) return LCB_ERR_ARG;
+  if (lse_head_stride < 0 || lse_batch_stride < 0 || lseb_head_stride < 0 || lseb_batch_stride < 0)
     return LCB_ERR_ARG;
-  if (lse_head_stride < 0 || lse_batch_stride < 0) return LCB_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return finish(launch_lse_merge(o_acc, lse_acc, o_b, o_b_dtype == LCB_DTYPE_F32, lse_b, o_out_bf16, B, H, rows,
-                                 o_row_stride, o_batch_stride, lse_head_stride, lse_batch_stride, st),
+                                 o_row_stride, o_batch_stride, ob_row_stride, ob_batch_stride, lse_head_stride,
+                                 lse_batch_stride, lseb_head_stride, lseb_batch_stride, st),
                 st);
 }
 

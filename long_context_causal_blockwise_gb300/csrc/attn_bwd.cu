@@ -22,6 +22,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "lcb_attn.h"
 #include "lcb_internal.h"
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 4 && lane == 0 && n > 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 4 && lane == 0 && n > 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -500,12 +501,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 int make_maps(const BwdLaunch& a, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tdo) {
   int rc;
   const int HD = a.H * kD;
-  // A dimension of size 0 cannot be described; such operands are never loaded.
-  const int sq = std::max(a.Sq, 1), sk = std::max(a.Sk, 1);
-  if ((rc = make_tma_map_bf16(tq, a.q, a.B, sq, HD, kT)) != 0) return rc;
-  if ((rc = make_tma_map_bf16(tdo, a.dO, a.B, sq, HD, kT)) != 0) return rc;
-  if ((rc = make_tma_map_bf16(tk, a.k, a.B, sk, HD, kT)) != 0) return rc;
-  if ((rc = make_tma_map_bf16(tv, a.v, a.B, sk, HD, kT)) != 0) return rc;
+  // An empty side is never loaded (the kernel's loop count is 0): its maps stay zeroed.
+  memset(tq, 0, sizeof(CUtensorMap));
+  memset(tdo, 0, sizeof(CUtensorMap));
+  memset(tk, 0, sizeof(CUtensorMap));
+  memset(tv, 0, sizeof(CUtensorMap));
+  if (a.Sq > 0) {
+    if ((rc = make_tma_map_bf16(tq, a.q, a.B, a.Sq, HD, kT)) != 0) return rc;
+    if ((rc = make_tma_map_bf16(tdo, a.dO, a.B, a.Sq, HD, kT)) != 0) return rc;
+  }
+  if (a.Sk > 0) {
+    if ((rc = make_tma_map_bf16(tk, a.k, a.B, a.Sk, HD, kT)) != 0) return rc;
+    if ((rc = make_tma_map_bf16(tv, a.v, a.B, a.Sk, HD, kT)) != 0) return rc;
+  }
   return 0;
 }
 

@@ -56,7 +56,9 @@ int launch_bwd_preprocess(const void* o, const void* dO, long long row_stride, l
 
 int launch_lse_merge(float* o_acc, float* lse_acc, const void* o_b, int o_b_f32, const float* lse_b, void* o_out_bf16,
                      int B, int H, int rows, long long o_row_stride, long long o_batch_stride,
-                     long long lse_head_stride, long long lse_batch_stride, cudaStream_t stream);
+                     long long ob_row_stride, long long ob_batch_stride, long long lse_head_stride,
+                     long long lse_batch_stride, long long lseb_head_stride, long long lseb_batch_stride,
+                     cudaStream_t stream);
 
 int launch_permute_rows(const void* src, void* dst, const int* perm, int rows, long long row_bytes, int scatter,
                         cudaStream_t stream);

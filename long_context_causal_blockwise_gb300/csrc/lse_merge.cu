@@ -32,7 +32,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(float* __restrict__ o_ac
                                                         const void* __restrict__ o_b, int o_b_f32,
                                                         const float* __restrict__ lse_b, __nv_bfloat16* o_out,
                                                         int B, int H, int rows, long long o_rs, long long o_bs,
-                                                        long long l_hs, long long l_bs) {
+                                                        long long ob_rs, long long ob_bs, long long l_hs,
+                                                        long long l_bs, long long lb_hs, long long lb_bs) {
   const long long n = static_cast<long long>(B) * rows * H;
   const int ln = threadIdx.x & 31;
   const long long wstep = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
@@ -42,13 +43,14 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(float* __restrict__ o_ac
     const int r = static_cast<int>(br % rows);
     const int b = static_cast<int>(br / rows);
     const long long off = b * o_bs + static_cast<long long>(r) * o_rs + h * kD + ln * 4;
+    const long long boff = b * ob_bs + static_cast<long long>(r) * ob_rs + h * kD + ln * 4;
     const long long loff = b * l_bs + h * l_hs + r;
     const float la = lse_acc[loff];
-    const float lb = __ldg(lse_b + loff);
+    const float lb = __ldg(lse_b + b * lb_bs + h * lb_hs + r);
     const float m = fmaxf(la, lb);
     float4 oa = *reinterpret_cast<const float4*>(o_acc + off);
-    float4 ob = o_b_f32 ? __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(o_b) + off))
-                        : load_bf16x4(static_cast<const __nv_bfloat16*>(o_b) + off);
+    float4 ob = o_b_f32 ? __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(o_b) + boff))
+                        : load_bf16x4(static_cast<const __nv_bfloat16*>(o_b) + boff);
     float4 out;
     float lse;
     if (m == -INFINITY) {
@@ -147,13 +149,16 @@ int grid_for(long long warps) {
 
 int launch_lse_merge(float* o_acc, float* lse_acc, const void* o_b, int o_b_f32, const float* lse_b, void* o_out_bf16,
                      int B, int H, int rows, long long o_row_stride, long long o_batch_stride,
-                     long long lse_head_stride, long long lse_batch_stride, cudaStream_t stream) {
+                     long long ob_row_stride, long long ob_batch_stride, long long lse_head_stride,
+                     long long lse_batch_stride, long long lseb_head_stride, long long lseb_batch_stride,
+                     cudaStream_t stream) {
   const long long warps = static_cast<long long>(B) * rows * H;
   if (warps == 0) return 0;
   lse_merge_kernel<<<grid_for(warps), 256, 0, stream>>>(o_acc, lse_acc, o_b, o_b_f32, lse_b,
                                                         static_cast<__nv_bfloat16*>(o_out_bf16), B, H, rows,
-                                                        o_row_stride, o_batch_stride, lse_head_stride,
-                                                        lse_batch_stride);
+                                                        o_row_stride, o_batch_stride, ob_row_stride,
+                                                        ob_batch_stride, lse_head_stride, lse_batch_stride,
+                                                        lseb_head_stride, lseb_batch_stride);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

@@ -71,8 +71,9 @@ def test_argument_errors_need_no_gpu(lib):
                            2048, 128, 2048, 128, 2048, 0, 16, 16, nul) == _lib.LCB_ERR_ARG
     # empty problems are no-ops
     assert lib.attn_fwd(nul, nul, nul, nul, nul, 1, 1, 0, 128, 1, 0.1, nul) == _lib.LCB_OK
-    assert lib.attn_lse_merge(nul, nul, nul, nul, 0, nul, 1, 1, 0, 128, 128, 0, 0, 0, nul) == _lib.LCB_OK
-    assert lib.attn_lse_merge(nul, nul, nul, nul, 7, nul, 1, 1, 4, 128, 128, 0, 0, 0, nul) == _lib.LCB_ERR_UNSUPPORTED
+    assert lib.attn_lse_merge(nul, nul, nul, nul, 0, nul, 1, 1, 0, 128, 128, 0, 128, 0, 0, 0, 0, 0, nul) == _lib.LCB_OK
+    assert lib.attn_lse_merge(nul, nul, nul, nul, 7, nul, 1, 1, 4, 128, 128, 0, 128, 0, 0, 0, 0, 0,
+                              nul) == _lib.LCB_ERR_UNSUPPORTED
     assert lib.attn_bwd_workspace_bytes(2, 3, 100, 128) >= 2 * 3 * 100 * 4
     assert lib.attn_bwd(nul, nul, nul, nul, nul, nul, nul, nul, nul, 1, 1, 16, 128, 1, 0.1, nul, 0,
                         nul) == _lib.LCB_ERR_ARG
