@@ -52,6 +52,7 @@ extern "C" {
 #define LCB_ERR_SCHEDULE (-3)    /* zigzag: P < 1 or S not a positive multiple of 2P */
 #define LCB_ERR_CUDA (-4)        /* a CUDA runtime/driver call or launch failed */
 #define LCB_ERR_TIMEOUT (-5)     /* checked mode: a device-side bounded wait expired */
+#define LCB_ERR_SCRATCH (-6)     /* attn_bwd_noalloc: B*H*S exceeds its fixed scratch */
 
 #define LCB_DTYPE_BF16 0
 #define LCB_DTYPE_F32 1
@@ -225,6 +226,35 @@ int lcb_selftest_bounded_wait(void* stream);
 /* Reads and clears the device status word of the current device (a
  * synchronising call): 0, or a bitmask with 1 = a bounded wait expired. */
 int lcb_take_device_status(unsigned int* where);
+
+/*
+ * attn_bwd_noalloc — attn_bwd for callers that cannot allocate device memory.
+ * The source pages have no counterpart of this call; it exists for callers
+ * that cannot hand the library a workspace, because their memory manager
+ * owns all device memory and gives out only the tensors they compute on,
+ * because their memory plan is fixed at start-up, or because they must not
+ * call cudaMalloc, which can synchronise the device mid-pipeline.
+ * Same arguments and results as attn_bwd minus the workspace. The Delta
+ * scratch lives in a fixed 8 MiB array in device memory inside the library;
+ * every GPU that loads the library holds it until the process exits.
+ *  - Limit: B * H * S <= attn_bwd_noalloc_max_rows() (2^21); larger problems
+ *    return LCB_ERR_SCRATCH and launch nothing.
+ *  - No allocation: the call makes no cudaMalloc/cudaFree or other
+ *    allocating call. Its first call on a device looks up the array's device
+ *    address (once per device); make that first call before any stream
+ *    capture.
+ *  - Sharing: every call uses the same array, which keeps the previous
+ *    call's contents. The call overwrites all the Delta values it reads, so
+ *    nothing needs clearing, but calls that overlap on the GPU (different
+ *    streams, or devices sharing nothing else) race on the array: order them
+ *    on one stream.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                     void* dq, void* dk, void* dv, int B, int H, int S, int D, int causal, float scale,
+                     void* stream);
+
+/* Largest B * H * S accepted by attn_bwd_noalloc. */
+long long attn_bwd_noalloc_max_rows(void);
 
 #ifdef __cplusplus
 }

@@ -3,7 +3,7 @@ training with sequence parallelism, as a C-ABI CUDA library (libattn.so) with a
 thin Python binding.
 
 Public calls (all run in this library's CUDA kernels):
-  attn_fwd, attn_fwd_ex, attn_bwd, attn_bwd_ex, attn_bwd_preprocess,
+  attn_fwd, attn_fwd_ex, attn_bwd, attn_bwd_ex, attn_bwd_preprocess, attn_bwd_noalloc,
   attn_lse_merge, zigzag_schedule, permute_rows, cast_f32_bf16,
   zigzag_attention_fwd / zigzag_attention_bwd (the one-device zigzag ring).
 
@@ -15,6 +15,8 @@ from ._lib import (  # noqa: F401
     AttnError,
     attn_bwd,
     attn_bwd_ex,
+    attn_bwd_noalloc,
+    attn_bwd_noalloc_max_rows,
     attn_bwd_preprocess,
     attn_bwd_workspace_bytes,
     attn_fwd,

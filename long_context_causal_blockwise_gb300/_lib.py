@@ -19,6 +19,7 @@ LCB_ERR_UNSUPPORTED = -2
 LCB_ERR_SCHEDULE = -3
 LCB_ERR_CUDA = -4
 LCB_ERR_TIMEOUT = -5
+LCB_ERR_SCRATCH = -6
 LCB_DTYPE_BF16 = 0
 LCB_DTYPE_F32 = 1
 LCB_GRAD_BF16 = 0
@@ -64,6 +65,8 @@ _SIGNATURES = {
     "lcb_scatter_rows": ([_P, _P, _P, _I, _LL, _P], _I),
     "lcb_cast_f32_bf16": ([_P, _P, _LL, _P], _I),
     "lcb_set_wait_limit_ns": ([_U64], _U64),
+    "attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P], _I),
+    "attn_bwd_noalloc_max_rows": ([], _LL),
     "lcb_selftest_bounded_wait": ([_P], _I),
     "lcb_take_device_status": ([ctypes.POINTER(ctypes.c_uint)], _I),
 }
@@ -196,6 +199,30 @@ def attn_bwd(q, k, v, o, lse, do, causal=True, scale=None, dq=None, dk=None, dv=
                                        _ptr(dv), B, H, S, D, int(causal), float(scale), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(q)))
     return dq, dk, dv
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, do, causal=True, scale=None, dq=None, dk=None, dv=None):
+    """attn_bwd without a workspace: Delta lives in the library's fixed device array.
+
+    For callers that cannot allocate device memory (see include/lcb_attn.h);
+    B*H*S must not exceed attn_bwd_noalloc_max_rows()."""
+    B, S, H, D = q.shape
+    scale = D ** -0.5 if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, torch.bfloat16, n, 4)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    _check("attn_bwd_noalloc", load().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                                       _ptr(dq), _ptr(dk), _ptr(dv), B, H, S, D, int(causal),
+                                                       float(scale), _stream(q)))
+    return dq, dk, dv
+
+
+def attn_bwd_noalloc_max_rows():
+    return int(load().attn_bwd_noalloc_max_rows())
 
 
 def attn_bwd_preprocess(o, do, delta):

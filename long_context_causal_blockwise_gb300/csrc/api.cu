@@ -138,6 +138,7 @@ const char* attn_status_string(int status) {
     case LCB_ERR_SCHEDULE: return "invalid zigzag schedule size";
     case LCB_ERR_CUDA: return "CUDA error";
     case LCB_ERR_TIMEOUT: return "device bounded wait expired";
+    case LCB_ERR_SCRATCH: return "problem larger than the fixed scratch of attn_bwd_noalloc (B*H*S > 2^21)";
     default: return "unknown status";
   }
 }
