@@ -8,24 +8,20 @@
 //   dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j.
 //
 // Two passes, each deterministic (no atomics):
-//   dK/dV pass: one CTA per 128-key tile, looping over query tiles.
-//     S^T = K Q^T and dP^T = V dO^T land in TMEM with one key per lane, so the
-//     per-query statistics (LSE, Delta) are columns, staged in shared memory.
-//     P^T and dS^T (bf16) overwrite S^T and dP^T in TMEM and feed
-//     dV += P^T dO and dK += dS^T Q directly from TMEM.
-//   dQ pass: one CTA per 128-query tile, looping over key tiles.
-//     S = Q K^T and dP = dO V^T with one query per lane; dS (bf16) overwrites
-//     S in TMEM and feeds dQ += dS K.
+//   dK/dV pass: one CTA per 128-key tile, looping over 128-query tiles.
+//   dQ pass:    one CTA per 128-query tile, looping over 128-key tiles.
 //
-// Each streamed 128-row tile is handled as two 64-row halves with their own
-// TMEM buffers and barriers: while the compute warps turn half h of one tile
-// into P/dS, the tensor core multiplies the other half, so elementwise work
-// and MMA overlap. Streamed operands arrive as 64-row half tiles in a 4-slot
-// ring, so a slot is refilled one full tile ahead of its use.
+// Every MMA is M=128 x N=128 x K=16: on this part a tcgen05.mma instruction
+// with N <= 128 costs about the same time whatever N is, so the work is issued
+// as few, full-width instructions. To keep the tensor core busy while the
+// compute warps turn scores into probabilities, a score buffer in TMEM is
+// released as soon as its values are in registers, and dS (the A operand of
+// dK or dQ) goes to shared memory in the 128-byte-swizzled K-major layout. The
+// next tile's score products then run during the elementwise work.
 //
-// Warps: 0-3 and 4-7 are two compute warpgroups, warpgroup h owning half h
-// (thread = TMEM lane = tile row); warp 8 is the TMA producer, warp 9 the MMA
-// issuer and TMEM owner.
+// Warps: 0-3 and 4-7 are two compute warpgroups (thread = TMEM lane = row of
+// the CTA's fixed tile); warpgroup x owns columns [64x, 64x+64) of each score
+// tile. Warp 8 is the TMA producer, warp 9 the MMA issuer and TMEM owner.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -37,41 +33,39 @@
 namespace lcb {
 namespace {
 
-constexpr int kT = 128;  // rows per tile (both query and key tiles)
-constexpr int kHalf = 64;
+constexpr int kT = 128;  // rows of every tile
 constexpr int kD = 128;
-constexpr int kThreads = 320;  // 8 compute warps (2 warpgroups), producer, MMA issuer
-constexpr uint32_t kTileBytes = kT * kD * 2;      // 32 KB: two 16 KB boxes of 128 rows x 64 columns
-constexpr uint32_t kTileColHalf = kTileBytes / 2;  // column-half stride inside a full tile
-constexpr uint32_t kHtBytes = kHalf * kD * 2;      // 16 KB half tile: two 8 KB boxes of 64 rows x 64 columns
-constexpr uint32_t kHtColHalf = kHtBytes / 2;      // column-half stride inside a half tile
-constexpr int kStages = 4;                         // ring slots, each (half tile A, half tile B) = 32 KB
+constexpr int kThreads = 320;
+constexpr int kCompute = 256;                    // compute threads
+constexpr uint32_t kTileBytes = kT * kD * 2;     // 32 KB: two 16 KB boxes of 128 rows x 64 columns
+constexpr uint32_t kColHalf = kTileBytes / 2;    // column-half stride of a tile
 constexpr float kLog2e = 1.4426950408889634f;
-
-// Fixed operands (2 full tiles), the ring, per-query stats, barriers.
-constexpr uint32_t kSmFixed = 0;
-constexpr uint32_t kSmRing = 2 * kTileBytes;
-constexpr uint32_t kSmStats = kSmRing + kStages * 2 * kHtBytes;  // [warpgroup][parity] x (lse2[64], delta[64]) fp32
-constexpr uint32_t kSmBar = kSmStats + 2 * 2 * kT * 4;
+constexpr int kMaxStages = 3;
 
 struct Bars {
-  uint64_t fixed_full;
-  uint64_t ring_full[kStages];
-  uint64_t ring_empty[kStages];
-  uint64_t s_full[2];      // per half: S (and dP) accumulated in TMEM
-  uint64_t p_full[2];      // per half: P / dS written back to TMEM
+  uint64_t fixed_full;  // the CTA's fixed operands are in place
+  uint64_t ring_full[kMaxStages];
+  uint64_t ring_empty[kMaxStages];
+  uint64_t s_full;    // S (S^T) computed
+  uint64_t dp_full;   // dP (dP^T) computed
+  uint64_t s_free;    // dQ pass: S and dP loaded by every compute thread
+  uint64_t dp_free;   // dK/dV pass: dP^T loaded by every compute thread
+  uint64_t p_full;    // P^T / dS written (TMEM and shared memory)
+  uint64_t ds_free;   // the MMA that read dS from shared memory completed
   uint64_t acc_full;
   uint64_t mma_done;
-  uint64_t stats_full[2][2];  // dK/dV pass: [warpgroup][parity], that warpgroup staged its LSE/Delta half
+  uint64_t stats_full[2];  // dK/dV pass: a warpgroup staged its LSE/Delta
   uint32_t tmem_base;
   int abort;
 };
-constexpr uint32_t kSmemBytes = kSmBar + sizeof(Bars) + 1024;
 
 struct Params {
   const float* lse;
   const float* delta;
   long long l_hs, l_bs;
+  const __nv_bfloat16* f0;  // dQ pass: Q and dO, written into TMEM as A operands
+  const __nv_bfloat16* f1;
+  long long f_rs, f_bs;
   void* g0;  // dK (dK/dV pass) or dQ (dQ pass)
   void* g1;  // dV (dK/dV pass)
   long long g_rs, g_bs;
@@ -90,79 +84,124 @@ __device__ bool drain_wait(uint64_t* bar, uint32_t parity, unsigned long long li
 
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
-__device__ __forceinline__ void init_bars(Bars* bars) {
-  mbar_init(&bars->fixed_full, 1);
-  for (int s = 0; s < kStages; ++s) {
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void init_bars(Bars* bars, int stages, uint32_t fixed_count) {
+  mbar_init(&bars->fixed_full, fixed_count);
+  for (int s = 0; s < stages; ++s) {
     mbar_init(&bars->ring_full[s], 1);
     mbar_init(&bars->ring_empty[s], 1);
   }
-  for (int h = 0; h < 2; ++h) {
-    mbar_init(&bars->s_full[h], 1);
-    mbar_init(&bars->p_full[h], kT);
-    mbar_init(&bars->stats_full[h][0], kT);
-    mbar_init(&bars->stats_full[h][1], kT);
-  }
+  mbar_init(&bars->s_full, 1);
+  mbar_init(&bars->dp_full, 1);
+  mbar_init(&bars->s_free, kCompute);
+  mbar_init(&bars->dp_free, kCompute);
+  mbar_init(&bars->p_full, kCompute);
+  mbar_init(&bars->ds_free, 1);
   mbar_init(&bars->acc_full, 1);
   mbar_init(&bars->mma_done, 1);
+  mbar_init(&bars->stats_full[0], kT);
+  mbar_init(&bars->stats_full[1], kT);
   bars->abort = 0;
   fence_mbar_init();
 }
 
-// Loads two fixed full tiles (rows f_row..f_row+127 of f0 and f1) once, then
-// ring items m = 0 .. 2n-1: the half tile of rows (first_tile + m/2)*128 +
-// (m%2)*64 of r0 and of r1.
-__device__ void producer(uint8_t* smem, Bars* bars, const CUtensorMap* f0, const CUtensorMap* f1, int f_row,
-                         const CUtensorMap* r0, const CUtensorMap* r1, int first_tile, int n, int h, int b,
-                         const Params& p, uint32_t where) {
+// Loads one 128-row tile (two 64-column boxes) of `map` at row `row`.
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int x0, int row, int b,
+                                          uint64_t pol) {
+  tma_load_3d_hint(dst, map, bar, x0, row, b, pol);
+  tma_load_3d_hint(dst + kColHalf, map, bar, x0 + 64, row, b, pol);
+}
+
+// Streams tiles i = 0 .. n-1 (rows (first_tile + i) * 128) of r0 and r1 into
+// ring slot i % kStages laid out [r0 tile][r1 tile].
+template <int kStages>
+__device__ void stream_tiles(uint8_t* ring, Bars* bars, const CUtensorMap* r0, const CUtensorMap* r1, int first_tile,
+                             int n, int h, int b, const Params& p, uint32_t where) {
   volatile int* abort_flag = &bars->abort;
   const int x0 = h * kD;
   const uint64_t pol = l2_policy_evict_last();
-  mbar_arrive_expect_tx(&bars->fixed_full, 2 * kTileBytes);
-  for (int c = 0; c < 2; ++c) {
-    tma_load_3d(smem + kSmFixed + c * kTileColHalf, f0, &bars->fixed_full, x0 + c * 64, f_row, b);
-    tma_load_3d(smem + kSmFixed + kTileBytes + c * kTileColHalf, f1, &bars->fixed_full, x0 + c * 64, f_row, b);
-  }
-  const int items = 2 * n;
-  int m = 0;
+  int i = 0;
   bool ok = true;
-  for (; m < items; ++m) {
-    const int s = m % kStages;
-    const uint32_t ph = static_cast<uint32_t>(m / kStages) & 1u;
+  for (; i < n; ++i) {
+    const int s = i % kStages;
+    const uint32_t ph = static_cast<uint32_t>(i / kStages) & 1u;
     if (!mbar_wait(&bars->ring_empty[s], ph ^ 1u, abort_flag, p.st, where | (1u << 16))) {
       ok = false;
       break;
     }
-    mbar_arrive_expect_tx(&bars->ring_full[s], 2 * kHtBytes);
-    const int row = (first_tile + (m >> 1)) * kT + (m & 1) * kHalf;
-    uint8_t* dst = smem + kSmRing + s * 2 * kHtBytes;
-    for (int c = 0; c < 2; ++c) {
-      tma_load_3d_hint(dst + c * kHtColHalf, r0, &bars->ring_full[s], x0 + c * 64, row, b, pol);
-      tma_load_3d_hint(dst + kHtBytes + c * kHtColHalf, r1, &bars->ring_full[s], x0 + c * 64, row, b, pol);
-    }
+    mbar_arrive_expect_tx(&bars->ring_full[s], 2 * kTileBytes);
+    uint8_t* dst = ring + s * 2 * kTileBytes;
+    const int row = (first_tile + i) * kT;
+    load_tile(dst, r0, &bars->ring_full[s], x0, row, b, pol);
+    load_tile(dst + kTileBytes, r1, &bars->ring_full[s], x0, row, b, pol);
   }
   if (!ok) {
-    drain_wait(&bars->fixed_full, 0, p.st.limit);
-    for (int k = std::max(0, m - kStages); k < m; ++k)
+    for (int k = std::max(0, i - kStages); k < i; ++k)
       drain_wait(&bars->ring_full[k % kStages], static_cast<uint32_t>(k / kStages) & 1u, p.st.limit);
   }
 }
 
-// D (128 x 64) = A (full tile, K-major) x B^T (half tile of 64 rows, K-major), contraction over D = 128.
-__device__ __forceinline__ void mma_full_x_half(uint32_t d, uint32_t a_base, uint32_t b_base, uint32_t idesc) {
+// Each thread copies row `row` (D = 128 bf16) of a fixed operand into TMEM as
+// A-operand columns (bf16 pairs, lane = row); rows past `rows` are zero.
+__device__ __forceinline__ void fixed_to_tmem(const __nv_bfloat16* base, long long rs, long long bs, int b, int h,
+                                              int row, int rows, uint32_t taddr) {
+  uint32_t w[64];
+  if (row < rows) {
+    const uint4* src = reinterpret_cast<const uint4*>(base + b * bs + static_cast<long long>(row) * rs + h * kD);
 #pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) {
-    const uint32_t a_off = (kk >> 2) * kTileColHalf + (kk & 3) * 32;
-    const uint32_t b_off = (kk >> 2) * kHtColHalf + (kk & 3) * 32;
-    mma_ss(d, sdesc_sw128(a_base + a_off, 16, 1024), sdesc_sw128(b_base + b_off, 16, 1024), idesc, kk > 0);
+    for (int i = 0; i < 16; ++i) {
+      const uint4 u = __ldg(src + i);
+      w[4 * i] = u.x;
+      w[4 * i + 1] = u.y;
+      w[4 * i + 2] = u.z;
+      w[4 * i + 3] = u.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) w[i] = 0u;
+  }
+  tmem_st_x64_nowait(taddr, w);
+}
+
+// D = A x B^T over K = 128, A and B 128-row K-major tiles in shared memory.
+__device__ __forceinline__ void mma_ss_tile(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t off = (kk >> 2) * kColHalf + (kk & 3) * 32;
+    mma_ss(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), idesc, (accumulate || kk > 0));
   }
 }
 
-// D (128 x 128) (+)= A (TMEM, 128 x 64 bf16 in 32 columns) x B (half tile [64 rows = K][128 = N], MN-major).
-__device__ __forceinline__ void mma_tmem_x_half(uint32_t d, uint32_t a_tmem, uint32_t b_base, uint32_t idesc,
-                                                bool accumulate) {
+// D = A x B^T over K = 128, A in TMEM (64 columns of bf16 pairs), B a K-major tile.
+__device__ __forceinline__ void mma_ts_tile(uint32_t d, uint32_t a_tmem, uint32_t b, uint32_t idesc) {
 #pragma unroll
-  for (int kk = 0; kk < kHalf / 16; ++kk) {
-    mma_ts(d, a_tmem + kk * 8, sdesc_sw128(b_base + kk * 2048, kHtColHalf, 1024), idesc, (accumulate || kk > 0));
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t off = (kk >> 2) * kColHalf + (kk & 3) * 32;
+    mma_ts(d, a_tmem + kk * 8, sdesc_sw128(b + off, 16, 1024), idesc, kk > 0);
+  }
+}
+
+// D (+)= A x B over K = 128, A a K-major tile in shared memory, B an MN-major tile [K rows][N = 128].
+__device__ __forceinline__ void mma_ss_tile_mn(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t a_off = (kk >> 2) * kColHalf + (kk & 3) * 32;
+    mma_ss(d, sdesc_sw128(a + a_off, 16, 1024), sdesc_sw128(b + kk * 2048, kColHalf, 1024), idesc,
+           (accumulate || kk > 0));
+  }
+}
+
+// Writes 64 bf16 values (32 packed words) as row `r`, column half `half` of a
+// 128 x 128 K-major tile with 128-byte swizzle (the layout TMA produces).
+__device__ __forceinline__ void st_tile_half_row(uint8_t* tile, int r, int half, const uint32_t (&w)[32]) {
+  uint8_t* rowp = tile + half * kColHalf + r * 128;
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
+        make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
   }
 }
 
@@ -198,29 +237,15 @@ __device__ __forceinline__ void store_grad_chunk(void* base, long long off, cons
   }
 }
 
-__device__ __forceinline__ void store_zero_row(void* base, long long off, int mode) {
+// Zeroes `cols` values of a gradient row (overwrite modes only).
+__device__ __forceinline__ void store_zero(void* base, long long off, int cols, int mode) {
   if (mode == LCB_GRAD_F32_ACCUM) return;
   if (mode == LCB_GRAD_BF16) {
     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off);
-#pragma unroll
-    for (int i = 0; i < kD / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 0; i < cols / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
   } else {
     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
-#pragma unroll
-    for (int i = 0; i < kD / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-}
-
-__device__ __forceinline__ void store_zero_half_row(void* base, long long off, int mode) {
-  if (mode == LCB_GRAD_F32_ACCUM) return;
-  if (mode == LCB_GRAD_BF16) {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off);
-#pragma unroll
-    for (int i = 0; i < kHalf / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-  } else {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
-#pragma unroll
-    for (int i = 0; i < kHalf / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < cols / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -231,20 +256,52 @@ __device__ __forceinline__ float lse2_of(const Params& p, int b, int h, int q) {
   return (l == -INFINITY) ? INFINITY : l * kLog2e;
 }
 
+__device__ __forceinline__ uint32_t start(Bars* bars, int stages, uint32_t fixed_count, int warp) {
+  if (threadIdx.x == 0) init_bars(bars, stages, fixed_count);
+  if (warp == 9) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  return bars->tmem_base;
+}
+
+__device__ __forceinline__ void teardown(uint32_t tbase, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
 // ============================================================== dK / dV pass
-// TMEM, per half h of the query tile: S^T_h [128h, 128h+64) (P^T_h bf16 in its
-// first 32 columns), dP^T_h [128h+64, 128h+128) (dS^T_h in its first 32).
-// dV [256,384), dK [384,512). Fixed tiles: K, V. Ring items: (Q half, dO half).
+// Shared memory: K, V (fixed, TMA), a 2-slot ring of (Q_i, dO_i), dS^T.
+// TMEM: S^T [0,128) (P^T bf16: queries 0-63 in [0,32), 64-127 in [64,96)),
+// dP^T [128,256), dV [256,384), dK [384,512).
+// MMA order per query tile i: dP^T(i+1) as soon as dP^T(i) is loaded; then,
+// once P^T(i)/dS^T(i) exist: dV += P^T dO_i, S^T(i+1), dK += dS^T Q_i.
+constexpr int kKvStages = 2;
+constexpr uint32_t kKvSmK = 0;
+constexpr uint32_t kKvSmV = kTileBytes;
+constexpr uint32_t kKvSmRing = 2 * kTileBytes;
+constexpr uint32_t kKvSmDs = kKvSmRing + kKvStages * 2 * kTileBytes;
+constexpr uint32_t kKvSmStats = kKvSmDs + kTileBytes;  // [wg] x (lse2[64], delta[64])
+constexpr uint32_t kKvSmBar = kKvSmStats + 2 * 2 * 64 * 4;
+constexpr uint32_t kKvSmem = kKvSmBar + sizeof(Bars) + 1024;
+
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                          const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  Bars* bars = reinterpret_cast<Bars*>(smem + kSmBar);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kKvSmBar);
   volatile int* abort_flag = &bars->abort;
-  float* stats = reinterpret_cast<float*>(smem + kSmStats);
+  float* stats = reinterpret_cast<float*>(smem + kKvSmStats);
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
   constexpr uint32_t kWhere = 2u << 24;
@@ -256,69 +313,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kt = static_cast<int>(blockIdx.x / BH);
   const int b = bh / p.H, h = bh % p.H;
   const int i0 = p.causal ? kt : 0;
-  const int n = std::max(0, nq - i0);
+  const int n = std::max(0, nq - i0);  // query tiles
 
-  if (threadIdx.x == 0) init_bars(bars);
-  if (warp == 9) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
-  }
-  if (warp == 8 && lane == 0 && n > 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_do);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = bars->tmem_base;
+  const uint32_t tbase = start(bars, kKvStages, 1, warp);
+  const uint32_t tS = tbase, tDP = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
 
   if (warp == 8) {
-    if (lane == 0 && n > 0) producer(smem, bars, &tm_k, &tm_v, kt * kT, &tm_q, &tm_do, i0, n, h, b, p, kWhere);
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      const uint64_t pol = l2_policy_evict_last();
+      mbar_arrive_expect_tx(&bars->fixed_full, 2 * kTileBytes);
+      load_tile(smem + kKvSmK, &tm_k, &bars->fixed_full, h * kD, kt * kT, b, pol);
+      load_tile(smem + kKvSmV, &tm_v, &bars->fixed_full, h * kD, kt * kT, b, pol);
+      stream_tiles<kKvStages>(smem + kKvSmRing, bars, &tm_q, &tm_do, i0, n, h, b, p, kWhere);
+    }
     __syncwarp();
   } else if (warp == 9) {
     if (lane == 0 && n > 0) {
-      const uint32_t id_s = idesc_bf16(kT, kHalf, false, false);  // 128 x 64 score half
-      const uint32_t id_g = idesc_bf16(kT, kD, false, true);      // 128 x 128 gradient update
-      const uint32_t sK = sbase + kSmFixed, sV = sbase + kSmFixed + kTileBytes;
-      auto item_q = [&](int m) { return sbase + kSmRing + (m % kStages) * 2 * kHtBytes; };
-      auto issue_scores = [&](int hh, int m) {  // S^T_h = K Q_h^T, dP^T_h = V dO_h^T
-        mma_full_x_half(tbase + 128 * hh, sK, item_q(m), id_s);
-        mma_full_x_half(tbase + 128 * hh + 64, sV, item_q(m) + kHtBytes, id_s);
-      };
-      auto wait_item = [&](int m) {
-        const bool r = mbar_wait(&bars->ring_full[m % kStages], static_cast<uint32_t>(m / kStages) & 1u, abort_flag,
-                                 p.st, kWhere | (3u << 16));
+      const uint32_t id_s = idesc_bf16(kT, kT, false, false);  // scores: both operands K-major
+      const uint32_t id_g = idesc_bf16(kT, kD, false, true);   // gradients: B MN-major
+      const uint32_t sK = sbase + kKvSmK, sV = sbase + kKvSmV, sDs = sbase + kKvSmDs;
+      auto slot = [&](int i) { return sbase + kKvSmRing + (i % kKvStages) * 2 * kTileBytes; };
+      auto wait_ring = [&](int i) {
+        const bool r = mbar_wait(&bars->ring_full[i % kKvStages], static_cast<uint32_t>(i / kKvStages) & 1u,
+                                 abort_flag, p.st, kWhere | (3u << 16));
         tc_fence_after();
         return r;
       };
       bool ok = mbar_wait(&bars->fixed_full, 0, abort_flag, p.st, kWhere | (2u << 16));
-      for (int hh = 0; hh < 2 && ok; ++hh) {
-        ok = wait_item(hh);
-        if (!ok) break;
-        issue_scores(hh, hh);
-        tc_commit(&bars->s_full[hh]);
+      if (ok) ok = wait_ring(0);
+      if (ok) {
+        mma_ss_tile(tS, sK, slot(0), id_s, false);  // S^T(0) = K Q_0^T
+        tc_commit(&bars->s_full);
+        mma_ss_tile(tDP, sV, slot(0) + kTileBytes, id_s, false);  // dP^T(0) = V dO_0^T
+        tc_commit(&bars->dp_full);
       }
-      for (int it = 0; it < n && ok; ++it) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          if (!ok) continue;
-          const int m = 2 * it + hh;
-          ok = mbar_wait(&bars->p_full[hh], static_cast<uint32_t>(it) & 1u, abort_flag, p.st, kWhere | (4u << 16));
-          if (!ok) continue;
+      for (int i = 0; i < n && ok; ++i) {
+        const uint32_t ph = static_cast<uint32_t>(i) & 1u;
+        if (i + 1 < n) {
+          ok = wait_ring(i + 1);
+          if (ok) ok = mbar_wait(&bars->dp_free, ph, abort_flag, p.st, kWhere | (8u << 16));
+          if (!ok) break;
           tc_fence_after();
-          const bool acc = it > 0 || hh > 0;
-          mma_tmem_x_half(tbase + 256, tbase + 128 * hh, item_q(m) + kHtBytes, id_g, acc);  // dV += P^T_h dO_h
-          mma_tmem_x_half(tbase + 384, tbase + 128 * hh + 64, item_q(m), id_g, acc);        // dK += dS^T_h Q_h
-          tc_commit(&bars->ring_empty[m % kStages]);
-          if (it + 1 < n) {
-            ok = wait_item(m + 2);
-            if (!ok) continue;
-            issue_scores(hh, m + 2);
-            tc_commit(&bars->s_full[hh]);
-          }
+          mma_ss_tile(tDP, sV, slot(i + 1) + kTileBytes, id_s, false);  // dP^T(i+1)
+          tc_commit(&bars->dp_full);
         }
+        ok = mbar_wait(&bars->p_full, ph, abort_flag, p.st, kWhere | (4u << 16));
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T(i) dO_i: P^T from TMEM (queries 0-63 at columns 0-31, 64-127 at 64-95)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t a = tS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          mma_ts(tDV, a, sdesc_sw128(slot(i) + kTileBytes + kk * 2048, kColHalf, 1024), id_g, (i > 0 || kk > 0));
+        }
+        if (i + 1 < n) {
+          mma_ss_tile(tS, sK, slot(i + 1), id_s, false);  // S^T(i+1), after the PV-type read of P^T(i)
+          tc_commit(&bars->s_full);
+        }
+        mma_ss_tile_mn(tDK, sDs, slot(i), id_g, i > 0);  // dK += dS^T(i) Q_i
+        tc_commit(&bars->ds_free);
+        tc_commit(&bars->ring_empty[i % kKvStages]);
       }
       if (ok) tc_commit(&bars->acc_full);
       tc_commit(&bars->mma_done);
@@ -327,106 +385,114 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- compute
-    const int hh = warp >> 2;          // this warpgroup's half of every query tile
+    const int x = warp >> 2;            // this warpgroup's query columns [64x, 64x + 64)
     const int row = threadIdx.x & 127;  // key row within the tile, TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tbase + lane_off + 128 * hh;
+    uint8_t* ds_tile = smem + kKvSmDs;
     const int j = kt * kT + row;
     const float c = p.scale_log2;
     bool ok = true;
-    for (int it = 0; it < n && ok; ++it) {
-      const int i = i0 + it;
-      const int qh = i * kT + hh * kHalf;  // first query of this half
-      float* buf = stats + (hh * 2 + (it & 1)) * 2 * kHalf;
-      if (row < kHalf) {
-        buf[row] = lse2_of(p, b, h, qh + row);
-        buf[kHalf + row] = (qh + row < p.Sq) ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + qh + row) : 0.f;
+    for (int i = 0; i < n && ok; ++i) {
+      const uint32_t ph = static_cast<uint32_t>(i) & 1u;
+      const int it = i0 + i;                // query tile
+      const int qh = it * kT + 64 * x;      // first query of this warpgroup's columns
+      float* buf = stats + x * 128;
+      // The buffer is single: every compute thread finished tile i-1 (p_full) before it is refilled.
+      if (i > 0) ok = warp_all(mbar_wait(&bars->p_full, ph ^ 1u, abort_flag, p.st, kWhere | (11u << 16)));
+      if (!ok) break;
+      const float l2v = row < 64 ? lse2_of(p, b, h, qh + row) : 0.f;
+      const float dlv = (row < 64 && qh + row < p.Sq) ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + qh + row) : 0.f;
+      if (row < 64) {
+        buf[row] = l2v;
+        buf[64 + row] = dlv;
       }
-      mbar_arrive(&bars->stats_full[hh][it & 1]);
-      ok = warp_all(mbar_wait(&bars->stats_full[hh][it & 1], static_cast<uint32_t>(it >> 1) & 1u, abort_flag, p.st,
-                              kWhere | (7u << 16)));
-      if (ok) {
-        ok = warp_all(
-            mbar_wait(&bars->s_full[hh], static_cast<uint32_t>(it) & 1u, abort_flag, p.st, kWhere | (5u << 16)));
-      }
+      mbar_arrive(&bars->stats_full[x]);
+      ok = warp_all(mbar_wait(&bars->stats_full[x], ph, abort_flag, p.st, kWhere | (7u << 16)));
+      if (ok) ok = warp_all(mbar_wait(&bars->s_full, ph, abort_flag, p.st, kWhere | (5u << 16)));
+      if (ok) ok = warp_all(mbar_wait(&bars->dp_full, ph, abort_flag, p.st, kWhere | (6u << 16)));
       if (!ok) break;
       tc_fence_after();
-      const bool diag = p.causal && (i == kt);
-#pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t s[32], dp[32];
-        tmem_ld2_x32(tS + ch * 32, tS + 64 + ch * 32, s, dp);
-        uint32_t pk[16], dk[16];
-        const int cb = ch * 32;  // query column within the half
+      uint32_t s[64], dp[64];
+      tmem_ld2_x64(tS + lane_off + 64 * x, tDP + lane_off + 64 * x, s, dp);
+      tc_fence_before();
+      mbar_arrive(&bars->dp_free);  // dP^T(i) is in registers: its TMEM may take dP^T(i+1)
+      const bool diag = p.causal && (it == kt);
+      uint32_t pk[32], dk[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 l2 = *reinterpret_cast<const float4*>(buf + cb + e);
-          const float4 dl = *reinterpret_cast<const float4*>(buf + kHalf + cb + e);
-          float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2.x));
-          float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -l2.y));
-          float p2 = ex2_approx(fmaf(__uint_as_float(s[e + 2]), c, -l2.z));
-          float p3 = ex2_approx(fmaf(__uint_as_float(s[e + 3]), c, -l2.w));
-          if (diag) {
-            const int q0 = qh + cb + e;
-            if (q0 < j) p0 = 0.f;
-            if (q0 + 1 < j) p1 = 0.f;
-            if (q0 + 2 < j) p2 = 0.f;
-            if (q0 + 3 < j) p3 = 0.f;
-          }
-          pk[e >> 1] = pack_bf16x2(p0, p1);
-          pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
-          dk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dl.x), p1 * (__uint_as_float(dp[e + 1]) - dl.y));
-          dk[(e >> 1) + 1] =
-              pack_bf16x2(p2 * (__uint_as_float(dp[e + 2]) - dl.z), p3 * (__uint_as_float(dp[e + 3]) - dl.w));
+      for (int e = 0; e < 64; e += 4) {
+        const float4 l2 = *reinterpret_cast<const float4*>(buf + e);
+        const float4 dl = *reinterpret_cast<const float4*>(buf + 64 + e);
+        float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2.x));
+        float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -l2.y));
+        float p2 = ex2_approx(fmaf(__uint_as_float(s[e + 2]), c, -l2.z));
+        float p3 = ex2_approx(fmaf(__uint_as_float(s[e + 3]), c, -l2.w));
+        if (diag) {
+          const int q0 = qh + e;
+          if (q0 < j) p0 = 0.f;
+          if (q0 + 1 < j) p1 = 0.f;
+          if (q0 + 2 < j) p2 = 0.f;
+          if (q0 + 3 < j) p3 = 0.f;
         }
-        tmem_st_x16_nowait(tS + ch * 16, pk);
-        tmem_st_x16_nowait(tS + 64 + ch * 16, dk);
+        pk[e >> 1] = pack_bf16x2(p0, p1);
+        pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
+        dk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dl.x), p1 * (__uint_as_float(dp[e + 1]) - dl.y));
+        dk[(e >> 1) + 1] =
+            pack_bf16x2(p2 * (__uint_as_float(dp[e + 2]) - dl.z), p3 * (__uint_as_float(dp[e + 3]) - dl.w));
       }
+      // P^T into this warpgroup's own S^T columns (already read by it).
+      tmem_st_x32_nowait(tS + lane_off + 64 * x, pk);
+      // dS^T into shared memory once the previous dK product has read it.
+      if (i > 0) {
+        ok = warp_all(mbar_wait(&bars->ds_free, (ph ^ 1u), abort_flag, p.st, kWhere | (9u << 16)));
+        if (!ok) break;
+      }
+      st_tile_half_row(ds_tile, row, x, dk);
+      fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->p_full[hh]);
+      mbar_arrive(&bars->p_full);
     }
     // Epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (scaled).
     const bool valid = j < p.Sk;
     const long long off = b * p.g_bs + static_cast<long long>(j) * p.g_rs + h * kD;
-    void* gdst = hh == 0 ? p.g1 : p.g0;
-    const float mul = hh == 0 ? 1.f : p.scale;
+    void* gdst = x == 0 ? p.g1 : p.g0;
+    const float mul = x == 0 ? 1.f : p.scale;
     if (n == 0) {
-      if (valid) store_zero_row(gdst, off, p.grad_mode);
+      if (valid) store_zero(gdst, off, kD, p.grad_mode);
     } else if (ok) {
-      ok = warp_all(mbar_wait(&bars->acc_full, 0, abort_flag, p.st, kWhere | (6u << 16)));
+      ok = warp_all(mbar_wait(&bars->acc_full, 0, abort_flag, p.st, kWhere | (10u << 16)));
       if (ok) {
         tc_fence_after();
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t a[32];
-          tmem_ld_x32(tbase + lane_off + 256 + 128 * hh + ch * 32, a);
+          tmem_ld_x32(tbase + lane_off + 256 + 128 * x + ch * 32, a);
           if (valid) store_grad_chunk(gdst, off + ch * 32, a, mul, p.grad_mode);
         }
       }
     }
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 9) {
-    tc_fence_after();
-    tmem_dealloc(tbase, 512);
-  }
+  teardown(tbase, warp);
 }
 
 // ============================================================== dQ pass
-// TMEM, per half h of the key tile: S_h [128h, 128h+64) (dS_h bf16 in its
-// first 32 columns), dP_h [128h+64, 128h+128); dQ [256,384).
-// Fixed tiles: Q, dO. Ring items: (K half, V half).
+// TMEM: Q [0,64) and dO [64,128) as A operands, S [128,256), dP [256,384),
+// dQ [384,512). Shared memory: a 3-slot ring of (K_j, V_j), dS.
+// MMA order per key tile j: S(j), dP(j) once S(j-1)/dP(j-1) are loaded;
+// then dQ += dS(j-1) K_{j-1}.
+constexpr int kQStages = 3;
+constexpr uint32_t kQSmRing = 0;
+constexpr uint32_t kQSmDs = kQStages * 2 * kTileBytes;
+constexpr uint32_t kQSmBar = kQSmDs + kTileBytes;
+constexpr uint32_t kQSmem = kQSmBar + sizeof(Bars) + 1024;
+
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  Bars* bars = reinterpret_cast<Bars*>(smem + kSmBar);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kQSmBar);
   volatile int* abort_flag = &bars->abort;
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
@@ -439,66 +505,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = blockIdx.x % BH;
   const int qt = nq - 1 - static_cast<int>(blockIdx.x / BH);
   const int b = bh / p.H, h = bh % p.H;
-  const int n = p.causal ? std::min(nk, qt + 1) : nk;
+  const int n = p.causal ? std::min(nk, qt + 1) : nk;  // key tiles
 
-  if (threadIdx.x == 0) init_bars(bars);
-  if (warp == 9) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
+  const uint32_t tbase = start(bars, kQStages, kCompute, warp);
+  const uint32_t tQ = tbase, tdO = tbase + 64, tS = tbase + 128, tDP = tbase + 256, tDQ = tbase + 384;
+
+  if (warp < 8 && n > 0) {
+    // Q (warpgroup 0) and dO (warpgroup 1) into TMEM, one row per thread.
+    const int wg = warp >> 2;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    fixed_to_tmem(wg == 0 ? p.f0 : p.f1, p.f_rs, p.f_bs, b, h, qt * kT + (threadIdx.x & 127), p.Sq,
+                  (wg == 0 ? tQ : tdO) + lane_off);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&bars->fixed_full);
   }
-  if (warp == 8 && lane == 0 && n > 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_do);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = bars->tmem_base;
 
   if (warp == 8) {
-    if (lane == 0 && n > 0) producer(smem, bars, &tm_q, &tm_do, qt * kT, &tm_k, &tm_v, 0, n, h, b, p, kWhere);
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      stream_tiles<kQStages>(smem + kQSmRing, bars, &tm_k, &tm_v, 0, n, h, b, p, kWhere);
+    }
     __syncwarp();
   } else if (warp == 9) {
     if (lane == 0 && n > 0) {
-      const uint32_t id_s = idesc_bf16(kT, kHalf, false, false);
+      const uint32_t id_s = idesc_bf16(kT, kT, false, false);
       const uint32_t id_g = idesc_bf16(kT, kD, false, true);
-      const uint32_t sQ = sbase + kSmFixed, sdO = sbase + kSmFixed + kTileBytes;
-      auto item_k = [&](int m) { return sbase + kSmRing + (m % kStages) * 2 * kHtBytes; };
-      auto issue_scores = [&](int hh, int m) {  // S_h = Q K_h^T, dP_h = dO V_h^T
-        mma_full_x_half(tbase + 128 * hh, sQ, item_k(m), id_s);
-        mma_full_x_half(tbase + 128 * hh + 64, sdO, item_k(m) + kHtBytes, id_s);
-      };
-      auto wait_item = [&](int m) {
-        const bool r = mbar_wait(&bars->ring_full[m % kStages], static_cast<uint32_t>(m / kStages) & 1u, abort_flag,
-                                 p.st, kWhere | (3u << 16));
-        tc_fence_after();
-        return r;
-      };
+      const uint32_t sDs = sbase + kQSmDs;
+      auto slot = [&](int j) { return sbase + kQSmRing + (j % kQStages) * 2 * kTileBytes; };
       bool ok = mbar_wait(&bars->fixed_full, 0, abort_flag, p.st, kWhere | (2u << 16));
-      for (int hh = 0; hh < 2 && ok; ++hh) {
-        ok = wait_item(hh);
-        if (!ok) break;
-        issue_scores(hh, hh);
-        tc_commit(&bars->s_full[hh]);
-      }
-      for (int it = 0; it < n && ok; ++it) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          if (!ok) continue;
-          const int m = 2 * it + hh;
-          ok = mbar_wait(&bars->p_full[hh], static_cast<uint32_t>(it) & 1u, abort_flag, p.st, kWhere | (4u << 16));
-          if (!ok) continue;
+      for (int j = 0; j <= n && ok; ++j) {
+        if (j < n) {
+          ok = mbar_wait(&bars->ring_full[j % kQStages], static_cast<uint32_t>(j / kQStages) & 1u, abort_flag, p.st,
+                         kWhere | (3u << 16));
+          if (ok && j > 0)
+            ok = mbar_wait(&bars->s_free, static_cast<uint32_t>(j - 1) & 1u, abort_flag, p.st, kWhere | (8u << 16));
+          if (!ok) break;
           tc_fence_after();
-          mma_tmem_x_half(tbase + 256, tbase + 128 * hh, item_k(m), id_g, it > 0 || hh > 0);  // dQ += dS_h K_h
-          tc_commit(&bars->ring_empty[m % kStages]);
-          if (it + 1 < n) {
-            ok = wait_item(m + 2);
-            if (!ok) continue;
-            issue_scores(hh, m + 2);
-            tc_commit(&bars->s_full[hh]);
-          }
+          mma_ts_tile(tS, tQ, slot(j), id_s);                // S(j)  = Q K_j^T
+          mma_ts_tile(tDP, tdO, slot(j) + kTileBytes, id_s);  // dP(j) = dO V_j^T
+          tc_commit(&bars->s_full);
+        }
+        if (j > 0) {
+          ok = mbar_wait(&bars->p_full, static_cast<uint32_t>(j - 1) & 1u, abort_flag, p.st, kWhere | (4u << 16));
+          if (!ok) break;
+          tc_fence_after();
+          mma_ss_tile_mn(tDQ, sDs, slot(j - 1), id_g, j > 1);  // dQ += dS(j-1) K_{j-1}
+          tc_commit(&bars->ds_free);
+          tc_commit(&bars->ring_empty[(j - 1) % kQStages]);
         }
       }
       if (ok) tc_commit(&bars->acc_full);
@@ -507,10 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    const int hh = warp >> 2;  // this warpgroup's half of every key tile
+    const int x = warp >> 2;  // this warpgroup's key columns [64x, 64x + 64)
     const int row = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tbase + lane_off + 128 * hh;
+    uint8_t* ds_tile = smem + kQSmDs;
     const int qi = qt * kT + row;
     const float c = p.scale_log2;
     const float l2 = lse2_of(p, b, h, qi);
@@ -518,82 +573,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q_first = qt * kT;
     const int lim = p.causal ? std::min(qi + 1, p.Sk) : p.Sk;  // keys < lim are visible
     bool ok = true;
-    for (int it = 0; it < n && ok; ++it) {
-      ok = warp_all(
-          mbar_wait(&bars->s_full[hh], static_cast<uint32_t>(it) & 1u, abort_flag, p.st, kWhere | (5u << 16)));
+    for (int j = 0; j < n && ok; ++j) {
+      const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+      ok = warp_all(mbar_wait(&bars->s_full, ph, abort_flag, p.st, kWhere | (5u << 16)));
       if (!ok) break;
       tc_fence_after();
-      const int kbase = it * kT + hh * kHalf;
-      const bool need_mask = (p.causal && kbase + kHalf - 1 > q_first) || (kbase + kHalf > p.Sk);
-#pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t s[32], dp[32];
-        tmem_ld2_x32(tS + ch * 32, tS + 64 + ch * 32, s, dp);
-        uint32_t ds[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2));
-          float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -l2));
-          if (need_mask) {
-            const int key = kbase + ch * 32 + e;
-            if (key >= lim) p0 = 0.f;
-            if (key + 1 >= lim) p1 = 0.f;
-          }
-          ds[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dl), p1 * (__uint_as_float(dp[e + 1]) - dl));
-        }
-        tmem_st_x16_nowait(tS + ch * 16, ds);
-      }
-      tmem_wait_st();
+      uint32_t s[64], dp[64];
+      tmem_ld2_x64(tS + lane_off + 64 * x, tDP + lane_off + 64 * x, s, dp);
       tc_fence_before();
-      mbar_arrive(&bars->p_full[hh]);
+      mbar_arrive(&bars->s_free);  // S(j), dP(j) are in registers: their TMEM may take S(j+1), dP(j+1)
+      const int kbase = j * kT + 64 * x;
+      const bool need_mask = (p.causal && kbase + 63 > q_first) || (kbase + 64 > p.Sk);
+      uint32_t ds[32];
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) {
+        float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2));
+        float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -l2));
+        if (need_mask) {
+          if (kbase + e >= lim) p0 = 0.f;
+          if (kbase + e + 1 >= lim) p1 = 0.f;
+        }
+        ds[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dl), p1 * (__uint_as_float(dp[e + 1]) - dl));
+      }
+      if (j > 0) {
+        ok = warp_all(mbar_wait(&bars->ds_free, ph ^ 1u, abort_flag, p.st, kWhere | (9u << 16)));
+        if (!ok) break;
+      }
+      st_tile_half_row(ds_tile, row, x, ds);
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->p_full);
     }
-    // Epilogue: warpgroup h writes dQ columns [64h, 64h + 64).
+    // Epilogue: warpgroup x writes dQ columns [64x, 64x + 64).
     const bool valid = qi < p.Sq;
-    const long long off = b * p.g_bs + static_cast<long long>(qi) * p.g_rs + h * kD + hh * kHalf;
+    const long long off = b * p.g_bs + static_cast<long long>(qi) * p.g_rs + h * kD + x * 64;
     if (n == 0) {
-      if (valid) store_zero_half_row(p.g0, off, p.grad_mode);
+      if (valid) store_zero(p.g0, off, 64, p.grad_mode);
     } else if (ok) {
-      ok = warp_all(mbar_wait(&bars->acc_full, 0, abort_flag, p.st, kWhere | (6u << 16)));
+      ok = warp_all(mbar_wait(&bars->acc_full, 0, abort_flag, p.st, kWhere | (10u << 16)));
       if (ok) {
         tc_fence_after();
 #pragma unroll 1
         for (int ch = 0; ch < 2; ++ch) {
           uint32_t a[32];
-          tmem_ld_x32(tbase + lane_off + 256 + hh * kHalf + ch * 32, a);
+          tmem_ld_x32(tDQ + lane_off + x * 64 + ch * 32, a);
           if (valid) store_grad_chunk(p.g0, off + ch * 32, a, p.scale, p.grad_mode);
         }
       }
     }
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 9) {
-    tc_fence_after();
-    tmem_dealloc(tbase, 512);
-  }
-}
-
-// Maps for one pass: the fixed operands use 128-row boxes, the streamed ones 64-row boxes.
-// An empty side is never loaded (the loop count is 0): its maps stay zeroed.
-int make_maps(const BwdLaunch& a, bool dkdv, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tdo) {
-  int rc;
-  const int HD = a.H * kD;
-  memset(tq, 0, sizeof(CUtensorMap));
-  memset(tdo, 0, sizeof(CUtensorMap));
-  memset(tk, 0, sizeof(CUtensorMap));
-  memset(tv, 0, sizeof(CUtensorMap));
-  const int q_box = dkdv ? kHalf : kT;
-  const int k_box = dkdv ? kT : kHalf;
-  if (a.Sq > 0) {
-    if ((rc = make_tma_map_bf16(tq, a.q, a.B, a.Sq, HD, q_box)) != 0) return rc;
-    if ((rc = make_tma_map_bf16(tdo, a.dO, a.B, a.Sq, HD, q_box)) != 0) return rc;
-  }
-  if (a.Sk > 0) {
-    if ((rc = make_tma_map_bf16(tk, a.k, a.B, a.Sk, HD, k_box)) != 0) return rc;
-    if ((rc = make_tma_map_bf16(tv, a.v, a.B, a.Sk, HD, k_box)) != 0) return rc;
-  }
-  return 0;
+  teardown(tbase, warp);
 }
 
 Params base_params(const BwdLaunch& a) {
@@ -602,6 +630,10 @@ Params base_params(const BwdLaunch& a) {
   p.delta = a.delta;
   p.l_hs = a.lse_head_stride;
   p.l_bs = a.lse_batch_stride;
+  p.f0 = nullptr;
+  p.f1 = nullptr;
+  p.f_rs = 0;
+  p.f_bs = 0;
   p.B = a.B;
   p.H = a.H;
   p.Sq = a.Sq;
@@ -618,12 +650,20 @@ Params base_params(const BwdLaunch& a) {
 
 int launch_attn_bwd_dkdv(const BwdLaunch& a, cudaStream_t stream) {
   if (a.Sk == 0) return 0;
-  CUtensorMap tq, tk, tv, tdo;
-  int rc = make_maps(a, true, &tq, &tk, &tv, &tdo);
-  if (rc != 0) return rc;
+  // An empty query side is never loaded (the kernel's loop count is 0): its maps stay zeroed.
+  CUtensorMap tk, tv, tq, tdo;
+  memset(&tq, 0, sizeof(tq));
+  memset(&tdo, 0, sizeof(tdo));
+  int rc;
+  if ((rc = make_tma_map_bf16(&tk, a.k, a.B, a.Sk, a.H * kD, kT)) != 0) return rc;
+  if ((rc = make_tma_map_bf16(&tv, a.v, a.B, a.Sk, a.H * kD, kT)) != 0) return rc;
+  if (a.Sq > 0) {
+    if ((rc = make_tma_map_bf16(&tq, a.q, a.B, a.Sq, a.H * kD, kT)) != 0) return rc;
+    if ((rc = make_tma_map_bf16(&tdo, a.dO, a.B, a.Sq, a.H * kD, kT)) != 0) return rc;
+  }
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+    if (cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem) !=
         cudaSuccess)
       return -4;
     attr = true;
@@ -635,30 +675,39 @@ int launch_attn_bwd_dkdv(const BwdLaunch& a, cudaStream_t stream) {
   p.g_bs = a.dkv_batch_stride;
   const long long grid = static_cast<long long>((a.Sk + kT - 1) / kT) * a.B * a.H;
   if (grid > 0x7fffffffLL) return -1;
-  attn_bwd_dkdv_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  attn_bwd_dkdv_kernel<<<static_cast<unsigned>(grid), kThreads, kKvSmem, stream>>>(tk, tv, tq, tdo, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 int launch_attn_bwd_dq(const BwdLaunch& a, cudaStream_t stream) {
   if (a.Sq == 0) return 0;
-  CUtensorMap tq, tk, tv, tdo;
-  int rc = make_maps(a, false, &tq, &tk, &tv, &tdo);
-  if (rc != 0) return rc;
+  CUtensorMap tk, tv;
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  int rc;
+  if (a.Sk > 0) {
+    if ((rc = make_tma_map_bf16(&tk, a.k, a.B, a.Sk, a.H * kD, kT)) != 0) return rc;
+    if ((rc = make_tma_map_bf16(&tv, a.v, a.B, a.Sk, a.H * kD, kT)) != 0) return rc;
+  }
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+    if (cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
         cudaSuccess)
       return -4;
     attr = true;
   }
   Params p = base_params(a);
+  p.f0 = static_cast<const __nv_bfloat16*>(a.q.ptr);
+  p.f1 = static_cast<const __nv_bfloat16*>(a.dO.ptr);
+  p.f_rs = a.q.row_stride;
+  p.f_bs = a.q.batch_stride;
   p.g0 = a.dq;
   p.g1 = nullptr;
   p.g_rs = a.dq_row_stride;
   p.g_bs = a.dq_batch_stride;
   const long long grid = static_cast<long long>((a.Sq + kT - 1) / kT) * a.B * a.H;
   if (grid > 0x7fffffffLL) return -1;
-  attn_bwd_dq_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  attn_bwd_dq_kernel<<<static_cast<unsigned>(grid), kThreads, kQSmem, stream>>>(tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
