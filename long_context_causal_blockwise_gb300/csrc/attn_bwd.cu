@@ -19,9 +19,9 @@
 // dK or dQ) goes to shared memory in the 128-byte-swizzled K-major layout. The
 // next tile's score products then run during the elementwise work.
 //
-// Warps: 0-3 and 4-7 are two compute warpgroups (thread = TMEM lane = row of
-// the CTA's fixed tile); warpgroup x owns columns [64x, 64x+64) of each score
-// tile. Warp 8 is the TMA producer, warp 9 the MMA issuer and TMEM owner.
+// Warps: 0-15 are four compute warpgroups (thread = TMEM lane = row of the
+// CTA's fixed tile); warpgroup x owns columns [32x, 32x+32) of each score
+// tile. Warp 16 is the TMA producer, warp 17 the MMA issuer and TMEM owner.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -35,8 +35,10 @@ namespace {
 
 constexpr int kT = 128;  // rows of every tile
 constexpr int kD = 128;
-constexpr int kThreads = 320;
-constexpr int kCompute = 256;                    // compute threads
+constexpr int kThreads = 576;                    // 16 compute warps, producer, MMA issuer
+constexpr int kCompute = 512;                    // compute threads
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
 constexpr uint32_t kTileBytes = kT * kD * 2;     // 32 KB: two 16 KB boxes of 128 rows x 64 columns
 constexpr uint32_t kColHalf = kTileBytes / 2;    // column-half stride of a tile
 constexpr float kLog2e = 1.4426950408889634f;
@@ -44,8 +46,10 @@ constexpr int kMaxStages = 3;
 
 struct Bars {
   uint64_t fixed_full;  // the CTA's fixed operands are in place
-  uint64_t ring_full[kMaxStages];
+  uint64_t ring_full[kMaxStages];  // dK/dV pass: the Q ring; dQ pass: the (K, V) ring
   uint64_t ring_empty[kMaxStages];
+  uint64_t do_full[2];  // dK/dV pass: the dO ring
+  uint64_t do_empty[2];
   uint64_t s_full;    // S (S^T) computed
   uint64_t dp_full;   // dP (dP^T) computed
   uint64_t s_free;    // dQ pass: S and dP loaded by every compute thread
@@ -54,7 +58,7 @@ struct Bars {
   uint64_t ds_free;   // the MMA that read dS from shared memory completed
   uint64_t acc_full;
   uint64_t mma_done;
-  uint64_t stats_full[2];  // dK/dV pass: a warpgroup staged its LSE/Delta
+  uint64_t stats_full[4];  // dK/dV pass: a warpgroup staged its LSE/Delta
   uint32_t tmem_base;
   int abort;
 };
@@ -102,8 +106,11 @@ __device__ __forceinline__ void init_bars(Bars* bars, int stages, uint32_t fixed
   mbar_init(&bars->ds_free, 1);
   mbar_init(&bars->acc_full, 1);
   mbar_init(&bars->mma_done, 1);
-  mbar_init(&bars->stats_full[0], kT);
-  mbar_init(&bars->stats_full[1], kT);
+  for (int x = 0; x < 4; ++x) mbar_init(&bars->stats_full[x], kT);
+  for (int s = 0; s < 2; ++s) {
+    mbar_init(&bars->do_full[s], 1);
+    mbar_init(&bars->do_empty[s], 1);
+  }
   bars->abort = 0;
   fence_mbar_init();
 }
@@ -205,6 +212,18 @@ __device__ __forceinline__ void st_tile_half_row(uint8_t* tile, int r, int half,
   }
 }
 
+// Writes 32 bf16 values (16 packed words) as columns [32q, 32q+32) of row `r`
+// of a 128 x 128 K-major tile with 128-byte swizzle.
+__device__ __forceinline__ void st_tile_quarter_row(uint8_t* tile, int r, int q, const uint32_t (&w)[16]) {
+  uint8_t* rowp = tile + (q >> 1) * kColHalf + r * 128;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int ch = 4 * (q & 1) + c;
+    *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
+        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  }
+}
+
 // Stores one 32-column chunk of a gradient row (fp32 accumulator values x mul).
 __device__ __forceinline__ void store_grad_chunk(void* base, long long off, const uint32_t (&a)[32], float mul,
                                                  int mode) {
@@ -258,7 +277,7 @@ __device__ __forceinline__ float lse2_of(const Params& p, int b, int h, int q) {
 
 __device__ __forceinline__ uint32_t start(Bars* bars, int stages, uint32_t fixed_count, int warp) {
   if (threadIdx.x == 0) init_bars(bars, stages, fixed_count);
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
@@ -271,25 +290,27 @@ __device__ __forceinline__ uint32_t start(Bars* bars, int stages, uint32_t fixed
 __device__ __forceinline__ void teardown(uint32_t tbase, int warp) {
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
 }
 
 // ============================================================== dK / dV pass
-// Shared memory: K, V (fixed, TMA), a 2-slot ring of (Q_i, dO_i), dS^T.
-// TMEM: S^T [0,128) (P^T bf16: queries 0-63 in [0,32), 64-127 in [64,96)),
-// dP^T [128,256), dV [256,384), dK [384,512).
+// Shared memory: K, V (fixed, TMA), a 2-slot Q ring, a 2-slot dO ring, dS^T.
+// TMEM: S^T [0,128) (P^T bf16: queries [32x, 32x+32) packed at columns
+// [32x, 32x+16)), dP^T [128,256), dV [256,384), dK [384,512).
 // MMA order per query tile i: dP^T(i+1) as soon as dP^T(i) is loaded; then,
-// once P^T(i)/dS^T(i) exist: dV += P^T dO_i, S^T(i+1), dK += dS^T Q_i.
+// once P^T(i)/dS^T(i) exist: dV += P^T dO_i (frees dO_i), S^T(i+1),
+// dK += dS^T Q_i (frees Q_i).
 constexpr int kKvStages = 2;
 constexpr uint32_t kKvSmK = 0;
 constexpr uint32_t kKvSmV = kTileBytes;
-constexpr uint32_t kKvSmRing = 2 * kTileBytes;
-constexpr uint32_t kKvSmDs = kKvSmRing + kKvStages * 2 * kTileBytes;
-constexpr uint32_t kKvSmStats = kKvSmDs + kTileBytes;  // [wg] x (lse2[64], delta[64])
-constexpr uint32_t kKvSmBar = kKvSmStats + 2 * 2 * 64 * 4;
+constexpr uint32_t kKvSmQ = 2 * kTileBytes;
+constexpr uint32_t kKvSmDo = kKvSmQ + kKvStages * kTileBytes;
+constexpr uint32_t kKvSmDs = kKvSmDo + kKvStages * kTileBytes;
+constexpr uint32_t kKvSmStats = kKvSmDs + kTileBytes;  // [wg] x (lse2[32], delta[32])
+constexpr uint32_t kKvSmBar = kKvSmStats + 4 * 64 * 4;
 constexpr uint32_t kKvSmem = kKvSmBar + sizeof(Bars) + 1024;
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -318,63 +339,100 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = start(bars, kKvStages, 1, warp);
   const uint32_t tS = tbase, tDP = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
 
-  if (warp == 8) {
+  if (warp == kProducerWarp) {
     if (lane == 0 && n > 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
+      const int x0 = h * kD;
       const uint64_t pol = l2_policy_evict_last();
       mbar_arrive_expect_tx(&bars->fixed_full, 2 * kTileBytes);
-      load_tile(smem + kKvSmK, &tm_k, &bars->fixed_full, h * kD, kt * kT, b, pol);
-      load_tile(smem + kKvSmV, &tm_v, &bars->fixed_full, h * kD, kt * kT, b, pol);
-      stream_tiles<kKvStages>(smem + kKvSmRing, bars, &tm_q, &tm_do, i0, n, h, b, p, kWhere);
+      load_tile(smem + kKvSmK, &tm_k, &bars->fixed_full, x0, kt * kT, b, pol);
+      load_tile(smem + kKvSmV, &tm_v, &bars->fixed_full, x0, kt * kT, b, pol);
+      // dO_i then Q_i, each into its own 2-slot ring.
+      int i = 0;
+      bool ok = true;
+      for (; i < n && ok; ++i) {
+        const int s = i % kKvStages;
+        const uint32_t ph = static_cast<uint32_t>(i / kKvStages) & 1u;
+        const int row = (i0 + i) * kT;
+        ok = mbar_wait(&bars->do_empty[s], ph ^ 1u, abort_flag, p.st, kWhere | (1u << 16));
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars->do_full[s], kTileBytes);
+        load_tile(smem + kKvSmDo + s * kTileBytes, &tm_do, &bars->do_full[s], x0, row, b, pol);
+        ok = mbar_wait(&bars->ring_empty[s], ph ^ 1u, abort_flag, p.st, kWhere | (1u << 16));
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars->ring_full[s], kTileBytes);
+        load_tile(smem + kKvSmQ + s * kTileBytes, &tm_q, &bars->ring_full[s], x0, row, b, pol);
+      }
+      if (!ok) {
+        drain_wait(&bars->fixed_full, 0, p.st.limit);
+        for (int k2 = std::max(0, i - kKvStages); k2 <= i && k2 < n; ++k2) {
+          const uint32_t ph2 = static_cast<uint32_t>(k2 / kKvStages) & 1u;
+          drain_wait(&bars->do_full[k2 % kKvStages], ph2, p.st.limit);
+          drain_wait(&bars->ring_full[k2 % kKvStages], ph2, p.st.limit);
+        }
+      }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0 && n > 0) {
       const uint32_t id_s = idesc_bf16(kT, kT, false, false);  // scores: both operands K-major
       const uint32_t id_g = idesc_bf16(kT, kD, false, true);   // gradients: B MN-major
       const uint32_t sK = sbase + kKvSmK, sV = sbase + kKvSmV, sDs = sbase + kKvSmDs;
-      auto slot = [&](int i) { return sbase + kKvSmRing + (i % kKvStages) * 2 * kTileBytes; };
-      auto wait_ring = [&](int i) {
+      auto q_slot = [&](int i) { return sbase + kKvSmQ + (i % kKvStages) * kTileBytes; };
+      auto do_slot = [&](int i) { return sbase + kKvSmDo + (i % kKvStages) * kTileBytes; };
+      auto wait_q = [&](int i) {
         const bool r = mbar_wait(&bars->ring_full[i % kKvStages], static_cast<uint32_t>(i / kKvStages) & 1u,
                                  abort_flag, p.st, kWhere | (3u << 16));
         tc_fence_after();
         return r;
       };
+      auto wait_do = [&](int i) {
+        const bool r = mbar_wait(&bars->do_full[i % kKvStages], static_cast<uint32_t>(i / kKvStages) & 1u,
+                                 abort_flag, p.st, kWhere | (12u << 16));
+        tc_fence_after();
+        return r;
+      };
       bool ok = mbar_wait(&bars->fixed_full, 0, abort_flag, p.st, kWhere | (2u << 16));
-      if (ok) ok = wait_ring(0);
+      if (ok) ok = wait_do(0);
       if (ok) {
-        mma_ss_tile(tS, sK, slot(0), id_s, false);  // S^T(0) = K Q_0^T
-        tc_commit(&bars->s_full);
-        mma_ss_tile(tDP, sV, slot(0) + kTileBytes, id_s, false);  // dP^T(0) = V dO_0^T
+        mma_ss_tile(tDP, sV, do_slot(0), id_s, false);  // dP^T(0) = V dO_0^T
         tc_commit(&bars->dp_full);
+      }
+      if (ok) ok = wait_q(0);
+      if (ok) {
+        mma_ss_tile(tS, sK, q_slot(0), id_s, false);  // S^T(0) = K Q_0^T
+        tc_commit(&bars->s_full);
       }
       for (int i = 0; i < n && ok; ++i) {
         const uint32_t ph = static_cast<uint32_t>(i) & 1u;
         if (i + 1 < n) {
-          ok = wait_ring(i + 1);
+          ok = wait_do(i + 1);
           if (ok) ok = mbar_wait(&bars->dp_free, ph, abort_flag, p.st, kWhere | (8u << 16));
           if (!ok) break;
           tc_fence_after();
-          mma_ss_tile(tDP, sV, slot(i + 1) + kTileBytes, id_s, false);  // dP^T(i+1)
+          mma_ss_tile(tDP, sV, do_slot(i + 1), id_s, false);  // dP^T(i+1)
           tc_commit(&bars->dp_full);
         }
         ok = mbar_wait(&bars->p_full, ph, abort_flag, p.st, kWhere | (4u << 16));
         if (!ok) break;
         tc_fence_after();
-        // dV += P^T(i) dO_i: P^T from TMEM (queries 0-63 at columns 0-31, 64-127 at 64-95)
+        // dV += P^T(i) dO_i; P^T K-step kk (queries 16kk..16kk+15) sits at columns 32(kk/2) + 8(kk%2)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t a = tS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tDV, a, sdesc_sw128(slot(i) + kTileBytes + kk * 2048, kColHalf, 1024), id_g, (i > 0 || kk > 0));
+          const uint32_t a = tS + 32 * (kk >> 1) + 8 * (kk & 1);
+          mma_ts(tDV, a, sdesc_sw128(do_slot(i) + kk * 2048, kColHalf, 1024), id_g, (i > 0 || kk > 0));
         }
+        tc_commit(&bars->do_empty[i % kKvStages]);
         if (i + 1 < n) {
-          mma_ss_tile(tS, sK, slot(i + 1), id_s, false);  // S^T(i+1), after the PV-type read of P^T(i)
+          ok = wait_q(i + 1);
+          if (!ok) break;
+          mma_ss_tile(tS, sK, q_slot(i + 1), id_s, false);  // S^T(i+1), after dV read P^T(i)
           tc_commit(&bars->s_full);
         }
-        mma_ss_tile_mn(tDK, sDs, slot(i), id_g, i > 0);  // dK += dS^T(i) Q_i
+        mma_ss_tile_mn(tDK, sDs, q_slot(i), id_g, i > 0);  // dK += dS^T(i) Q_i
         tc_commit(&bars->ds_free);
         tc_commit(&bars->ring_empty[i % kKvStages]);
       }
@@ -385,26 +443,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- compute
-    const int x = warp >> 2;            // this warpgroup's query columns [64x, 64x + 64)
+    const int x = warp >> 2;            // this warpgroup's query columns [32x, 32x + 32)
     const int row = threadIdx.x & 127;  // key row within the tile, TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint8_t* ds_tile = smem + kKvSmDs;
+    float* buf = stats + x * 64;
     const int j = kt * kT + row;
     const float c = p.scale_log2;
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
       const uint32_t ph = static_cast<uint32_t>(i) & 1u;
-      const int it = i0 + i;                // query tile
-      const int qh = it * kT + 64 * x;      // first query of this warpgroup's columns
-      float* buf = stats + x * 128;
-      // The buffer is single: every compute thread finished tile i-1 (p_full) before it is refilled.
+      const int it = i0 + i;            // query tile
+      const int qx = it * kT + 32 * x;  // first query of this warpgroup's columns
+      // The stats buffer is single: every compute thread finished tile i-1 (p_full) before it is refilled.
       if (i > 0) ok = warp_all(mbar_wait(&bars->p_full, ph ^ 1u, abort_flag, p.st, kWhere | (11u << 16)));
       if (!ok) break;
-      const float l2v = row < 64 ? lse2_of(p, b, h, qh + row) : 0.f;
-      const float dlv = (row < 64 && qh + row < p.Sq) ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + qh + row) : 0.f;
-      if (row < 64) {
-        buf[row] = l2v;
-        buf[64 + row] = dlv;
+      if (row < 32) {
+        buf[row] = lse2_of(p, b, h, qx + row);
+        buf[32 + row] = (qx + row < p.Sq) ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + qx + row) : 0.f;
       }
       mbar_arrive(&bars->stats_full[x]);
       ok = warp_all(mbar_wait(&bars->stats_full[x], ph, abort_flag, p.st, kWhere | (7u << 16)));
@@ -412,22 +468,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = warp_all(mbar_wait(&bars->dp_full, ph, abort_flag, p.st, kWhere | (6u << 16)));
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[64], dp[64];
-      tmem_ld2_x64(tS + lane_off + 64 * x, tDP + lane_off + 64 * x, s, dp);
+      uint32_t s[32], dp[32];
+      tmem_ld2_x32(tS + lane_off + 32 * x, tDP + lane_off + 32 * x, s, dp);
       tc_fence_before();
       mbar_arrive(&bars->dp_free);  // dP^T(i) is in registers: its TMEM may take dP^T(i+1)
       const bool diag = p.causal && (it == kt);
-      uint32_t pk[32], dk[32];
+      uint32_t pk[16], dk[16];
 #pragma unroll
-      for (int e = 0; e < 64; e += 4) {
+      for (int e = 0; e < 32; e += 4) {
         const float4 l2 = *reinterpret_cast<const float4*>(buf + e);
-        const float4 dl = *reinterpret_cast<const float4*>(buf + 64 + e);
+        const float4 dl = *reinterpret_cast<const float4*>(buf + 32 + e);
         float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2.x));
         float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -l2.y));
         float p2 = ex2_approx(fmaf(__uint_as_float(s[e + 2]), c, -l2.z));
         float p3 = ex2_approx(fmaf(__uint_as_float(s[e + 3]), c, -l2.w));
         if (diag) {
-          const int q0 = qh + e;
+          const int q0 = qx + e;
           if (q0 < j) p0 = 0.f;
           if (q0 + 1 < j) p1 = 0.f;
           if (q0 + 2 < j) p2 = 0.f;
@@ -440,33 +496,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             pack_bf16x2(p2 * (__uint_as_float(dp[e + 2]) - dl.z), p3 * (__uint_as_float(dp[e + 3]) - dl.w));
       }
       // P^T into this warpgroup's own S^T columns (already read by it).
-      tmem_st_x32_nowait(tS + lane_off + 64 * x, pk);
+      tmem_st_x16_nowait(tS + lane_off + 32 * x, pk);
       // dS^T into shared memory once the previous dK product has read it.
       if (i > 0) {
-        ok = warp_all(mbar_wait(&bars->ds_free, (ph ^ 1u), abort_flag, p.st, kWhere | (9u << 16)));
+        ok = warp_all(mbar_wait(&bars->ds_free, ph ^ 1u, abort_flag, p.st, kWhere | (9u << 16)));
         if (!ok) break;
       }
-      st_tile_half_row(ds_tile, row, x, dk);
+      st_tile_quarter_row(ds_tile, row, x, dk);
       fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full);
     }
-    // Epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (scaled).
+    // Epilogue: warpgroups 0/1 write dV columns [0,64)/[64,128), 2/3 write dK (scaled).
     const bool valid = j < p.Sk;
-    const long long off = b * p.g_bs + static_cast<long long>(j) * p.g_rs + h * kD;
-    void* gdst = x == 0 ? p.g1 : p.g0;
-    const float mul = x == 0 ? 1.f : p.scale;
+    const int half = x & 1;
+    const long long off = b * p.g_bs + static_cast<long long>(j) * p.g_rs + h * kD + 64 * half;
+    void* gdst = x < 2 ? p.g1 : p.g0;
+    const float mul = x < 2 ? 1.f : p.scale;
+    const uint32_t tacc = (x < 2 ? tDV : tDK) + lane_off + 64 * half;
     if (n == 0) {
-      if (valid) store_zero(gdst, off, kD, p.grad_mode);
+      if (valid) store_zero(gdst, off, 64, p.grad_mode);
     } else if (ok) {
       ok = warp_all(mbar_wait(&bars->acc_full, 0, abort_flag, p.st, kWhere | (10u << 16)));
       if (ok) {
         tc_fence_after();
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 0; ch < 2; ++ch) {
           uint32_t a[32];
-          tmem_ld_x32(tbase + lane_off + 256 + 128 * x + ch * 32, a);
+          tmem_ld_x32(tacc + ch * 32, a);
           if (valid) store_grad_chunk(gdst, off + ch * 32, a, mul, p.grad_mode);
         }
       }
@@ -507,11 +565,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / p.H, h = bh % p.H;
   const int n = p.causal ? std::min(nk, qt + 1) : nk;  // key tiles
 
-  const uint32_t tbase = start(bars, kQStages, kCompute, warp);
+  const uint32_t tbase = start(bars, kQStages, 256, warp);
   const uint32_t tQ = tbase, tdO = tbase + 64, tS = tbase + 128, tDP = tbase + 256, tDQ = tbase + 384;
 
   if (warp < 8 && n > 0) {
-    // Q (warpgroup 0) and dO (warpgroup 1) into TMEM, one row per thread.
+    // Q (warps 0-3) and dO (warps 4-7) into TMEM, one row per thread.
     const int wg = warp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     fixed_to_tmem(wg == 0 ? p.f0 : p.f1, p.f_rs, p.f_bs, b, h, qt * kT + (threadIdx.x & 127), p.Sq,
@@ -521,14 +579,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_arrive(&bars->fixed_full);
   }
 
-  if (warp == 8) {
+  if (warp == kProducerWarp) {
     if (lane == 0 && n > 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       stream_tiles<kQStages>(smem + kQSmRing, bars, &tm_k, &tm_v, 0, n, h, b, p, kWhere);
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0 && n > 0) {
       const uint32_t id_s = idesc_bf16(kT, kT, false, false);
       const uint32_t id_g = idesc_bf16(kT, kD, false, true);
@@ -562,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    const int x = warp >> 2;  // this warpgroup's key columns [64x, 64x + 64)
+    const int x = warp >> 2;  // this warpgroup's key columns [32x, 32x + 32)
     const int row = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint8_t* ds_tile = smem + kQSmDs;
@@ -578,15 +636,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_all(mbar_wait(&bars->s_full, ph, abort_flag, p.st, kWhere | (5u << 16)));
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[64], dp[64];
-      tmem_ld2_x64(tS + lane_off + 64 * x, tDP + lane_off + 64 * x, s, dp);
+      uint32_t s[32], dp[32];
+      tmem_ld2_x32(tS + lane_off + 32 * x, tDP + lane_off + 32 * x, s, dp);
       tc_fence_before();
       mbar_arrive(&bars->s_free);  // S(j), dP(j) are in registers: their TMEM may take S(j+1), dP(j+1)
-      const int kbase = j * kT + 64 * x;
-      const bool need_mask = (p.causal && kbase + 63 > q_first) || (kbase + 64 > p.Sk);
-      uint32_t ds[32];
+      const int kbase = j * kT + 32 * x;
+      const bool need_mask = (p.causal && kbase + 31 > q_first) || (kbase + 32 > p.Sk);
+      uint32_t ds[16];
 #pragma unroll
-      for (int e = 0; e < 64; e += 2) {
+      for (int e = 0; e < 32; e += 2) {
         float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2));
         float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -l2));
         if (need_mask) {
@@ -599,25 +657,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = warp_all(mbar_wait(&bars->ds_free, ph ^ 1u, abort_flag, p.st, kWhere | (9u << 16)));
         if (!ok) break;
       }
-      st_tile_half_row(ds_tile, row, x, ds);
+      st_tile_quarter_row(ds_tile, row, x, ds);
       fence_proxy_async_smem();
       mbar_arrive(&bars->p_full);
     }
-    // Epilogue: warpgroup x writes dQ columns [64x, 64x + 64).
+    // Epilogue: warpgroup x writes dQ columns [32x, 32x + 32).
     const bool valid = qi < p.Sq;
-    const long long off = b * p.g_bs + static_cast<long long>(qi) * p.g_rs + h * kD + x * 64;
+    const long long off = b * p.g_bs + static_cast<long long>(qi) * p.g_rs + h * kD + x * 32;
     if (n == 0) {
-      if (valid) store_zero(p.g0, off, 64, p.grad_mode);
+      if (valid) store_zero(p.g0, off, 32, p.grad_mode);
     } else if (ok) {
       ok = warp_all(mbar_wait(&bars->acc_full, 0, abort_flag, p.st, kWhere | (10u << 16)));
       if (ok) {
         tc_fence_after();
-#pragma unroll 1
-        for (int ch = 0; ch < 2; ++ch) {
-          uint32_t a[32];
-          tmem_ld_x32(tDQ + lane_off + x * 64 + ch * 32, a);
-          if (valid) store_grad_chunk(p.g0, off + ch * 32, a, p.scale, p.grad_mode);
-        }
+        uint32_t a[32];
+        tmem_ld_x32(tDQ + lane_off + x * 32, a);
+        if (valid) store_grad_chunk(p.g0, off, a, p.scale, p.grad_mode);
       }
     }
   }
