@@ -78,13 +78,6 @@ struct Params {
   DevStatus st;
 };
 
-__device__ bool drain_wait(uint64_t* bar, uint32_t parity, unsigned long long limit) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit) return false;
-  }
-  return true;
-}
 
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 

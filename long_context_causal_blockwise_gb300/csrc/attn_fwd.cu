@@ -88,14 +88,6 @@ __device__ __forceinline__ void tile_counts(const Params& p, int q0, int& n0, in
 
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
-// Waits for the barrier ignoring the abort flag (used to drain in-flight copies).
-__device__ bool drain_wait(uint64_t* bar, uint32_t parity, unsigned long long limit) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit) return false;
-  }
-  return true;
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,

@@ -72,25 +72,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or about `hint_ns` pass, instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint32_t kSleepHintNs = 1000000;  // 1 ms between abort/time-limit checks
+
 // Bounded wait for the phase with the given parity. Returns false if the CTA's
 // abort flag is raised or the limit passes; in the latter case the thread
 // raises the abort flag and records the timeout in the device status word.
-// Every thread that calls this polls; callers make the outcome warp-uniform.
+// Every thread that calls this waits; callers make the outcome warp-uniform.
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                            const DevStatus& st, uint32_t where) {
+                                                   const DevStatus& st, uint32_t where) {
   const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > st.limit) {
-        *abort_flag = 1;
-        if (atomicOr(st.words, DEV_TIMEOUT) == 0) {
-          st.words[1] = where | ((blockIdx.x & 0xffu)) | ((warp_id() & 0xffu) << 8);
-          st.words[2] = blockIdx.x;
-        }
-        return false;
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > st.limit) {
+      *abort_flag = 1;
+      if (atomicOr(st.words, DEV_TIMEOUT) == 0) {
+        st.words[1] = where | ((blockIdx.x & 0xffu)) | ((warp_id() & 0xffu) << 8);
+        st.words[2] = blockIdx.x;
       }
+      return false;
     }
   }
 }
@@ -99,6 +113,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
                                           const DevStatus& st, uint32_t where) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, abort_flag, st, where);
+}
+
+// Waits for the phase ignoring the abort flag, up to `limit` ns (used to let
+// in-flight copies and MMAs finish before a CTA exits).
+__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity, unsigned long long limit) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
+    if (globaltimer_ns() - t0 > limit) return false;
+  }
+  return true;
 }
 
 // ---------------------------------------------------------------- TMA
