@@ -443,6 +443,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* buf = stats + x * 64;
     const int j = kt * kT + row;
     const float c = p.scale_log2;
+    // LSE/Delta of the tile's 32 queries of this warpgroup, loaded one tile ahead (threads 0-31).
+    auto load_stats = [&](int i, float& l2v, float& dlv) {
+      const int q = (i0 + i) * kT + 32 * x + row;
+      l2v = lse2_of(p, b, h, q);
+      dlv = (q < p.Sq) ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + q) : 0.f;
+    };
+    float nl2 = 0.f, ndl = 0.f;
+    if (row < 32 && n > 0) load_stats(0, nl2, ndl);
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
       const uint32_t ph = static_cast<uint32_t>(i) & 1u;
@@ -452,8 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (i > 0) ok = warp_all(mbar_wait(&bars->p_full, ph ^ 1u, abort_flag, p.st, kWhere | (11u << 16)));
       if (!ok) break;
       if (row < 32) {
-        buf[row] = lse2_of(p, b, h, qx + row);
-        buf[32 + row] = (qx + row < p.Sq) ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + qx + row) : 0.f;
+        buf[row] = nl2;
+        buf[32 + row] = ndl;
+        if (i + 1 < n) load_stats(i + 1, nl2, ndl);
       }
       mbar_arrive(&bars->stats_full[x]);
       ok = warp_all(mbar_wait(&bars->stats_full[x], ph, abort_flag, p.st, kWhere | (7u << 16)));

@@ -230,8 +230,11 @@ def attn_key_rows(q, k, v, do, keys, heads, causal, scale):
     """dK and dV for a sample of key rows on a subset of heads, every batch.
 
     dK_j and dV_j sum over all query rows i, and each term needs LSE_i and
-    Delta_i, i.e. the whole softmax row i. Every query row is therefore
-    formed in full (in panels); only the sampled key columns are reduced.
+    Delta_i, i.e. the whole softmax row i. Every query row that can see a
+    sampled key is therefore formed in full (in panels); only the sampled key
+    columns are reduced. When causal, query rows i < min(keys) see none of the
+    sampled keys (P_ij = 0 for j > i) and are skipped, so keys sampled near the
+    end of a long sequence are cheap.
     Returns (dk [B,K,len(heads),D], dv [B,K,len(heads),D]).
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
@@ -240,10 +243,11 @@ def attn_key_rows(q, k, v, do, keys, heads, causal, scale):
     dk = np.zeros((B, len(keys), len(heads), D))
     dv = np.zeros((B, len(keys), len(heads), D))
     step = _panel_rows(Sk)
+    first = int(keys.min()) if (causal and len(keys)) else 0
     for b in range(B):
         for hi, h in enumerate(heads):
             kh, vh = k[b, :, h, :], v[b, :, h, :]
-            for r0 in range(0, Sq, step):
+            for r0 in range(first, Sq, step):
                 rows = np.arange(r0, min(Sq, r0 + step))
                 qh, doh = q[b, rows, h, :], do[b, rows, h, :]
                 p, _ = _softmax_rows(scale * (qh @ kh.T), _visible(rows, Sk, causal))

@@ -246,6 +246,11 @@ def test_sampled_rows_agree_with_full():
     dk, dv = oracle.attn_key_rows(q, k, v, do, keys, [1], True, 0.3)
     np.testing.assert_allclose(dk[:, :, 0], full["dk"][:, keys, 1], atol=1e-12)
     np.testing.assert_allclose(dv[:, :, 0], full["dv"][:, keys, 1], atol=1e-12)
+    # tail keys: only query rows at or after the first sampled key are formed
+    tail = np.array([40, 44, 49])
+    dk, dv = oracle.attn_key_rows(q, k, v, do, tail, [0, 1], True, 0.3)
+    np.testing.assert_allclose(dk, full["dk"][:, tail], atol=1e-12)
+    np.testing.assert_allclose(dv, full["dv"][:, tail], atol=1e-12)
 
 
 def test_empty_rows():
