@@ -54,11 +54,11 @@ struct Bars {
   uint64_t dp_full;   // dP (dP^T) computed
   uint64_t s_free;    // dQ pass: S and dP loaded by every compute thread
   uint64_t dp_free;   // dK/dV pass: dP^T loaded by every compute thread
-  uint64_t p_full;    // P^T / dS written (TMEM and shared memory)
+  uint64_t p_full;    // dS written to shared memory (dK/dV pass: dS^T)
+  uint64_t pt_full;   // dK/dV pass: P^T written to TMEM
   uint64_t ds_free;   // the MMA that read dS from shared memory completed
   uint64_t acc_full;
   uint64_t mma_done;
-  uint64_t stats_full[4];  // dK/dV pass: a warpgroup staged its LSE/Delta
   uint32_t tmem_base;
   int abort;
 };
@@ -96,10 +96,10 @@ __device__ __forceinline__ void init_bars(Bars* bars, int stages, uint32_t fixed
   mbar_init(&bars->s_free, kCompute);
   mbar_init(&bars->dp_free, kCompute);
   mbar_init(&bars->p_full, kCompute);
+  mbar_init(&bars->pt_full, kCompute);
   mbar_init(&bars->ds_free, 1);
   mbar_init(&bars->acc_full, 1);
   mbar_init(&bars->mma_done, 1);
-  for (int x = 0; x < 4; ++x) mbar_init(&bars->stats_full[x], kT);
   for (int s = 0; s < 2; ++s) {
     mbar_init(&bars->do_full[s], 1);
     mbar_init(&bars->do_empty[s], 1);
@@ -302,8 +302,7 @@ constexpr uint32_t kKvSmV = kTileBytes;
 constexpr uint32_t kKvSmQ = 2 * kTileBytes;
 constexpr uint32_t kKvSmDo = kKvSmQ + kKvStages * kTileBytes;
 constexpr uint32_t kKvSmDs = kKvSmDo + kKvStages * kTileBytes;
-constexpr uint32_t kKvSmStats = kKvSmDs + kTileBytes;  // [wg] x (lse2[32], delta[32])
-constexpr uint32_t kKvSmBar = kKvSmStats + 4 * 64 * 4;
+constexpr uint32_t kKvSmBar = kKvSmDs + kTileBytes;
 constexpr uint32_t kKvSmem = kKvSmBar + sizeof(Bars) + 1024;
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -315,7 +314,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   Bars* bars = reinterpret_cast<Bars*>(smem + kKvSmBar);
   volatile int* abort_flag = &bars->abort;
-  float* stats = reinterpret_cast<float*>(smem + kKvSmStats);
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
   constexpr uint32_t kWhere = 2u << 24;
@@ -409,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss_tile(tDP, sV, do_slot(i + 1), id_s, false);  // dP^T(i+1)
           tc_commit(&bars->dp_full);
         }
-        ok = mbar_wait(&bars->p_full, ph, abort_flag, p.st, kWhere | (4u << 16));
+        ok = mbar_wait(&bars->pt_full, ph, abort_flag, p.st, kWhere | (4u << 16));
         if (!ok) break;
         tc_fence_after();
         // dV += P^T(i) dO_i; P^T K-step kk (queries 16kk..16kk+15) sits at columns 32(kk/2) + 8(kk%2)
@@ -425,6 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss_tile(tS, sK, q_slot(i + 1), id_s, false);  // S^T(i+1), after dV read P^T(i)
           tc_commit(&bars->s_full);
         }
+        ok = mbar_wait(&bars->p_full, ph, abort_flag, p.st, kWhere | (13u << 16));
+        if (!ok) break;
+        tc_fence_after();
         mma_ss_tile_mn(tDK, sDs, q_slot(i), id_g, i > 0);  // dK += dS^T(i) Q_i
         tc_commit(&bars->ds_free);
         tc_commit(&bars->ring_empty[i % kKvStages]);
@@ -440,33 +441,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = threadIdx.x & 127;  // key row within the tile, TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint8_t* ds_tile = smem + kKvSmDs;
-    float* buf = stats + x * 64;
     const int j = kt * kT + row;
     const float c = p.scale_log2;
-    // LSE/Delta of the tile's 32 queries of this warpgroup, loaded one tile ahead (threads 0-31).
+    // Lane l holds LSE2/Delta of query 32x + l of a tile (loaded a tile ahead);
+    // every thread reads all 32 through warp shuffles.
     auto load_stats = [&](int i, float& l2v, float& dlv) {
-      const int q = (i0 + i) * kT + 32 * x + row;
+      const int q = (i0 + i) * kT + 32 * x + lane;
       l2v = lse2_of(p, b, h, q);
       dlv = (q < p.Sq) ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + q) : 0.f;
     };
     float nl2 = 0.f, ndl = 0.f;
-    if (row < 32 && n > 0) load_stats(0, nl2, ndl);
+    if (n > 0) load_stats(0, nl2, ndl);
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
       const uint32_t ph = static_cast<uint32_t>(i) & 1u;
       const int it = i0 + i;            // query tile
       const int qx = it * kT + 32 * x;  // first query of this warpgroup's columns
-      // The stats buffer is single: every compute thread finished tile i-1 (p_full) before it is refilled.
-      if (i > 0) ok = warp_all(mbar_wait(&bars->p_full, ph ^ 1u, abort_flag, p.st, kWhere | (11u << 16)));
-      if (!ok) break;
-      if (row < 32) {
-        buf[row] = nl2;
-        buf[32 + row] = ndl;
-        if (i + 1 < n) load_stats(i + 1, nl2, ndl);
-      }
-      mbar_arrive(&bars->stats_full[x]);
-      ok = warp_all(mbar_wait(&bars->stats_full[x], ph, abort_flag, p.st, kWhere | (7u << 16)));
-      if (ok) ok = warp_all(mbar_wait(&bars->s_full, ph, abort_flag, p.st, kWhere | (5u << 16)));
+      const float l2v = nl2, dlv = ndl;
+      if (i + 1 < n) load_stats(i + 1, nl2, ndl);
+      ok = warp_all(mbar_wait(&bars->s_full, ph, abort_flag, p.st, kWhere | (5u << 16)));
       if (ok) ok = warp_all(mbar_wait(&bars->dp_full, ph, abort_flag, p.st, kWhere | (6u << 16)));
       if (!ok) break;
       tc_fence_after();
@@ -475,39 +468,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->dp_free);  // dP^T(i) is in registers: its TMEM may take dP^T(i+1)
       const bool diag = p.causal && (it == kt);
-      uint32_t pk[16], dk[16];
+      // Phase 1: P^T, into this warpgroup's own S^T columns (already read by it).
+      float pv[32];
+      uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        const float4 l2 = *reinterpret_cast<const float4*>(buf + e);
-        const float4 dl = *reinterpret_cast<const float4*>(buf + 32 + e);
-        float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2.x));
-        float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -l2.y));
-        float p2 = ex2_approx(fmaf(__uint_as_float(s[e + 2]), c, -l2.z));
-        float p3 = ex2_approx(fmaf(__uint_as_float(s[e + 3]), c, -l2.w));
-        if (diag) {
-          const int q0 = qx + e;
-          if (q0 < j) p0 = 0.f;
-          if (q0 + 1 < j) p1 = 0.f;
-          if (q0 + 2 < j) p2 = 0.f;
-          if (q0 + 3 < j) p3 = 0.f;
-        }
-        pk[e >> 1] = pack_bf16x2(p0, p1);
-        pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
-        dk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dl.x), p1 * (__uint_as_float(dp[e + 1]) - dl.y));
-        dk[(e >> 1) + 1] =
-            pack_bf16x2(p2 * (__uint_as_float(dp[e + 2]) - dl.z), p3 * (__uint_as_float(dp[e + 3]) - dl.w));
+      for (int e = 0; e < 32; ++e) {
+        const float l2 = __shfl_sync(0xffffffffu, l2v, e);
+        float pe = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2));
+        if (diag && qx + e < j) pe = 0.f;
+        pv[e] = pe;
       }
-      // P^T into this warpgroup's own S^T columns (already read by it).
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(pv[e], pv[e + 1]);
       tmem_st_x16_nowait(tS + lane_off + 32 * x, pk);
-      // dS^T into shared memory once the previous dK product has read it.
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->pt_full);  // dV(i) and S^T(i+1) may go
+      // Phase 2: dS^T = P^T (dP^T - Delta), into shared memory for dK.
+      uint32_t dk[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const float d0 = __shfl_sync(0xffffffffu, dlv, e);
+        const float d1 = __shfl_sync(0xffffffffu, dlv, e + 1);
+        dk[e >> 1] = pack_bf16x2(pv[e] * (__uint_as_float(dp[e]) - d0), pv[e + 1] * (__uint_as_float(dp[e + 1]) - d1));
+      }
       if (i > 0) {
         ok = warp_all(mbar_wait(&bars->ds_free, ph ^ 1u, abort_flag, p.st, kWhere | (9u << 16)));
         if (!ok) break;
       }
       st_tile_quarter_row(ds_tile, row, x, dk);
       fence_proxy_async_smem();
-      tmem_wait_st();
-      tc_fence_before();
       mbar_arrive(&bars->p_full);
     }
     // Epilogue: warpgroups 0/1 write dV columns [0,64)/[64,128), 2/3 write dK (scaled).
