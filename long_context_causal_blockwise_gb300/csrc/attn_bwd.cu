@@ -318,11 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = static_cast<int>(lane_id());
   constexpr uint32_t kWhere = 2u << 24;
 
-  // Work item: key tile kt of (b, h); causal work shrinks with kt, so low kt first.
+  // Work item: key tile kt of (b, h). Head-major order: the CTAs running at once
+  // belong to one or two heads, so the query tiles they all stream stay in L2;
+  // within a head, causal work shrinks with kt, so low kt first.
   const int nq = (p.Sq + kT - 1) / kT;
-  const int BH = p.B * p.H;
-  const int bh = blockIdx.x % BH;
-  const int kt = static_cast<int>(blockIdx.x / BH);
+  const int nkt = (p.Sk + kT - 1) / kT;
+  const int bh = static_cast<int>(blockIdx.x / nkt);
+  const int kt = static_cast<int>(blockIdx.x % nkt);
   const int b = bh / p.H, h = bh % p.H;
   const int i0 = p.causal ? kt : 0;
   const int n = std::max(0, nq - i0);  // query tiles
@@ -548,12 +550,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = static_cast<int>(lane_id());
   constexpr uint32_t kWhere = 3u << 24;
 
-  // Work item: query tile qt of (b, h); causal work grows with qt, so high qt first.
+  // Work item: query tile qt of (b, h). Head-major order (the key tiles every
+  // running CTA streams stay in L2); within a head, causal work grows with qt,
+  // so high qt first.
   const int nq = (p.Sq + kT - 1) / kT;
   const int nk = (p.Sk + kT - 1) / kT;
-  const int BH = p.B * p.H;
-  const int bh = blockIdx.x % BH;
-  const int qt = nq - 1 - static_cast<int>(blockIdx.x / BH);
+  const int bh = static_cast<int>(blockIdx.x / nq);
+  const int qt = nq - 1 - static_cast<int>(blockIdx.x % nq);
   const int b = bh / p.H, h = bh % p.H;
   const int n = p.causal ? std::min(nk, qt + 1) : nk;  // key tiles
 

@@ -102,11 +102,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
 
-  // Work item: heaviest (latest) query blocks first across all heads.
+  // Work item: query block qblk of (b, h). Head-major order (the K/V tiles every
+  // running CTA streams stay in L2); within a head the heaviest (latest) query
+  // blocks go first.
   const int nq = (p.Sq + 2 * kBM - 1) / (2 * kBM);
-  const int BH = p.B * p.H;
-  const int bh = blockIdx.x % BH;
-  const int qblk = nq - 1 - static_cast<int>(blockIdx.x / BH);
+  const int bh = static_cast<int>(blockIdx.x / nq);
+  const int qblk = nq - 1 - static_cast<int>(blockIdx.x % nq);
   const int b = bh / p.H;
   const int h = bh % p.H;
   const int q0 = qblk * 2 * kBM;
