@@ -54,6 +54,42 @@ def fwd_flop(b, h, s, d):
     return 2.0 * b * h * s * s * d
 
 
+def kernel_source_hash(files):
+    """sha256 over the kernel sources a recorded ncu figure was taken from."""
+    import hashlib
+
+    hsh = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "long_context_causal_blockwise_gb300", "csrc", f), "rb") as fh:
+            hsh.update(fh.read())
+    return hsh.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "attn_fwd": ("attn_fwd.cu", "common.cuh", "tmem_ldst.cuh"),
+    "bwd_dkdv": ("attn_bwd.cu", "common.cuh", "tmem_ldst.cuh"),
+    "bwd_dq": ("attn_bwd.cu", "common.cuh", "tmem_ldst.cuh"),
+    "bwd_preprocess": ("lse_merge.cu", "common.cuh"),
+}
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch at this workload from a committed ncu record
+    (profiles/dram_traffic_b1h32s32768.txt), or None when the record is missing
+    or was taken from a different version of the kernel's sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_b1h32s32768.txt")
+    try:
+        want = kernel_source_hash(KERNEL_SOURCES[kernel])
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 3 and parts[0] == kernel and parts[1] == want:
+                    return int(parts[2])
+    except (OSError, KeyError, ValueError):
+        return None
+    return None
+
+
 def load_peaks():
     """(tensor TFLOP/s sustained, tensor burst, HBM GB/s, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -304,11 +340,13 @@ def run_ours(args, rank, world, local_rank):
     if kind == "tensor":
         ach = work / avg[dom] / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": sus, "unit": "TFLOP/s", "frac": ach / sus,
-                "traffic": None, "peak_source": f"{src} bf16 sustained"}
+                "traffic": recorded_traffic(dom) if (H, S) == (32, 32768) else None,
+                "peak_source": f"{src} bf16 sustained"}
     else:
         ach = work / avg[dom] / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "traffic": None, "peak_source": f"{src} HBM copy"}
+                "traffic": recorded_traffic(dom) if (H, S) == (32, 32768) else None,
+                "peak_source": f"{src} HBM copy"}
     fwd_t = avg["attn_fwd"]
     bwd_t = avg["bwd_preprocess"] + avg["bwd_dkdv"] + avg["bwd_dq"]
     line = {
@@ -348,7 +386,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--H", type=int, default=H, help="heads (profiling of smaller cases only)")
     ap.add_argument("--S", type=int, default=S, help="sequence length (profiling of smaller cases only)")
+    ap.add_argument("--print-kernel-hashes", action="store_true",
+                    help="print the source hash of each kernel (for recording ncu traffic) and exit")
     args = ap.parse_args()
+    if args.print_kernel_hashes:
+        for k, files in KERNEL_SOURCES.items():
+            print(k, kernel_source_hash(files))
+        return 0
     if (args.H, args.S) != (H, S):
         _set_shape(args.H, args.S)
     world = int(os.environ.get("WORLD_SIZE", "1"))
