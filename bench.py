@@ -377,6 +377,82 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+def run_zigzag(args):
+    """Times the one-device zigzag ring (S = 131072, P = 8, H = 32) against
+    monolithic attention on the same inputs; prints one JSON line (not the
+    headline bench line)."""
+    import torch
+
+    import long_context_causal_blockwise_gb300 as lcb
+    from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo
+    from long_context_causal_blockwise_gb300.zigzag import ZigzagPlan
+
+    Hz, Sz, Pz = 32, 131072, 8
+    dev = torch.device("cuda", 0)
+    lcb.load()
+    q, k, v, do = gaussian_qkvdo(1, Hz, Sz, D, seed=0, device=dev)
+    plan = ZigzagPlan(Sz, Pz, dev)
+    c2 = Sz // Pz
+    bufs = {
+        "o_acc": torch.empty(1, Sz, Hz, D, device=dev), "lse": torch.empty(1, Hz, Sz, device=dev),
+        "o_blk": torch.empty(1, c2, Hz, D, device=dev, dtype=torch.bfloat16),
+        "lse_blk": torch.empty(1, Hz, c2, device=dev), "o": torch.empty_like(q),
+    }
+    g32 = tuple(torch.empty(1, Sz, Hz, D, device=dev) for _ in range(3))
+    g16 = tuple(torch.empty_like(q) for _ in range(3))
+    delta = torch.empty(1, Hz, Sz, device=dev)
+    qz, kz, vz, doz = (plan.gather(x) for x in (q, k, v, do))
+
+    def ring_fwd(fused=True):
+        return lcb.zigzag_attention_fwd(qz, kz, vz, plan, fused=fused, **bufs)
+
+    def ring():
+        o, lse, _ = ring_fwd()
+        lcb.zigzag_attention_bwd(qz, kz, vz, o, lse, doz, plan, delta=delta, grads32=g32, grads=g16)
+
+    o_m, lse_m = torch.empty_like(q), torch.empty(1, Hz, Sz, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(lcb.attn_bwd_workspace_bytes(1, Hz, Sz, D), dtype=torch.uint8, device=dev)
+
+    def mono():
+        lcb.attn_fwd(q, k, v, o=o_m, lse=lse_m)
+        lcb.attn_bwd(q, k, v, o_m, lse_m, do, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    steps = max(1, min(args.steps, 5))
+    t_ring, t_mono = timed(ring, steps), timed(mono, steps)
+    t_fwd_fused, t_fwd_unfused = timed(ring_fwd, steps), timed(lambda: ring_fwd(False), steps)
+    t_fwd_mono = timed(lambda: lcb.attn_fwd(q, k, v, o=o_m, lse=lse_m), steps)
+    # merge kernel alone: one LOWER/UPPER-sized merge (2c rows) timed in isolation
+    oa, la = bufs["o_acc"][:, :c2], bufs["lse"][:, :, :c2]
+    ob, lb = bufs["o_blk"], bufs["lse_blk"]
+    t_merge = timed(lambda: lcb.attn_lse_merge(oa, la, ob, lb), 20)
+    merge_bytes = c2 * Hz * (D * 4 * 2 + D * 2 + 12)
+    _, _, hbm, src = load_peaks()
+    flop = step_flop(1, Hz, Sz, D)
+    print(json.dumps({
+        "metric": "zigzag ring emulation fwd+bwd (P=8, S=131072, H=32, D=128) vs monolithic",
+        "ring_ms": t_ring, "monolithic_ms": t_mono, "ring_overhead_pct": 100.0 * (t_ring / t_mono - 1.0),
+        "ring_tflops": flop / t_ring / 1e9, "monolithic_tflops": flop / t_mono / 1e9,
+        "fwd_ms": {"ring_fused_merge": t_fwd_fused, "ring_merge_kernel": t_fwd_unfused, "monolithic": t_fwd_mono},
+        "merge_ms_per_call": t_merge, "merge_rows": c2, "merge_gbs": merge_bytes / t_merge / 1e6,
+        "merge_frac_of_hbm": merge_bytes / t_merge / 1e6 / hbm, "hbm_peak_source": src,
+        "launches_per_ring_step": "fwd: 1 (merge fused in the epilogue); bwd: 2 per task + 1 preprocess"}),
+          flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -386,9 +462,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--H", type=int, default=H, help="heads (profiling of smaller cases only)")
     ap.add_argument("--S", type=int, default=S, help="sequence length (profiling of smaller cases only)")
+    ap.add_argument("--zigzag", action="store_true",
+                    help="time the one-device zigzag ring (S=131072, P=8) against monolithic attention")
     ap.add_argument("--print-kernel-hashes", action="store_true",
                     help="print the source hash of each kernel (for recording ncu traffic) and exit")
     args = ap.parse_args()
+    if args.zigzag:
+        return run_zigzag(args)
     if args.print_kernel_hashes:
         for k, files in KERNEL_SOURCES.items():
             print(k, kernel_source_hash(files))

@@ -56,6 +56,9 @@ extern "C" {
 
 #define LCB_DTYPE_BF16 0
 #define LCB_DTYPE_F32 1
+/* attn_fwd_ex output mode: fold the block's (O, LSE) into an fp32 ring
+ * accumulator held in o and lse (a fused ring step). */
+#define LCB_OUT_F32_MERGE 2
 
 /* How attn_bwd_ex writes dq/dk/dv. */
 #define LCB_GRAD_BF16 0      /* bf16, overwritten */
@@ -96,8 +99,11 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * Queries have Sq rows, keys/values Sk rows (Sq != Sk only when causal == 0).
  * Strides are in elements: row stride between consecutive tokens, batch stride
  * between batches; q and o share nothing but shape. o_dtype selects bf16 or
- * fp32 output. lse strides: between heads and between batches.
- * Sk == 0 writes O = 0 and LSE = -inf.
+ * fp32 output, or LCB_OUT_F32_MERGE: o (fp32) and lse already hold a partial
+ * result over other keys, and this block's result is merged into them in the
+ * kernel's epilogue exactly as attn_lse_merge would (a fused ring step, [SP]).
+ * lse strides: between heads and between batches.
+ * Sk == 0 writes O = 0 and LSE = -inf (merge mode: leaves o, lse unchanged).
  */
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk,
                 int D, int causal, float scale, long long q_row_stride, long long q_batch_stride,

@@ -22,6 +22,7 @@ LCB_ERR_TIMEOUT = -5
 LCB_ERR_SCRATCH = -6
 LCB_DTYPE_BF16 = 0
 LCB_DTYPE_F32 = 1
+LCB_OUT_F32_MERGE = 2
 LCB_GRAD_BF16 = 0
 LCB_GRAD_F32_ACCUM = 1
 LCB_GRAD_F32_STORE = 2
@@ -157,8 +158,11 @@ def attn_fwd(q, k, v, causal=True, scale=None, o=None, lse=None):
     return o, lse
 
 
-def attn_fwd_ex(q, k, v, o, lse, causal, scale):
-    """Forward on strided [B,S,H,D] views; o bf16 or fp32; lse [B,H,Sq] view."""
+def attn_fwd_ex(q, k, v, o, lse, causal, scale, merge=False):
+    """Forward on strided [B,S,H,D] views; o bf16 or fp32; lse [B,H,Sq] view.
+
+    merge=True: o (fp32) and lse hold a partial result over other keys and this
+    block is merged into them in the kernel (a fused ring step)."""
     B, Sq, H, D = q.shape
     Sk = k.shape[1]
     qr, qb = _bshd(q, "q")
@@ -167,6 +171,10 @@ def attn_fwd_ex(q, k, v, o, lse, causal, scale):
     if (vr, vb) != (kr, kb):
         raise ValueError("k and v must share strides")
     o_dtype = LCB_DTYPE_F32 if o.dtype == torch.float32 else LCB_DTYPE_BF16
+    if merge:
+        if o.dtype != torch.float32:
+            raise ValueError("merge mode needs an fp32 accumulator")
+        o_dtype = LCB_OUT_F32_MERGE
     orr, ob = _bshd(o, "o", o.dtype)
     lh, lb = _bhs(lse, "lse")
     _check("attn_fwd_ex", load().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk, D,

@@ -166,7 +166,7 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
   if (causal != 0 && causal != 1) return LCB_ERR_ARG;
   if (causal && Sq != Sk) return LCB_ERR_UNSUPPORTED;
-  if (o_dtype != LCB_DTYPE_BF16 && o_dtype != LCB_DTYPE_F32) return LCB_ERR_UNSUPPORTED;
+  if (o_dtype != LCB_DTYPE_BF16 && o_dtype != LCB_DTYPE_F32 && o_dtype != LCB_OUT_F32_MERGE) return LCB_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !std::isfinite(scale)) return LCB_ERR_ARG;
   if (Sq == 0) return LCB_OK;
   if (!o || !lse || !aligned16(o)) return LCB_ERR_ARG;
@@ -175,6 +175,7 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   if (static_cast<long long>(H) * kHeadDim > o_row_stride) return LCB_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (Sk == 0) {
+    if (o_dtype == LCB_OUT_F32_MERGE) return LCB_OK;  // an empty block leaves the accumulator unchanged
     return finish(launch_fill_empty(o, o_dtype == LCB_DTYPE_F32, o_row_stride, o_batch_stride, lse, lse_head_stride,
                                     lse_batch_stride, B, H, Sq, st),
                   st);
@@ -200,7 +201,7 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   a.Sq = Sq;
   a.Sk = Sk;
   a.causal = causal;
-  a.o_f32 = o_dtype == LCB_DTYPE_F32;
+  a.o_mode = o_dtype == LCB_OUT_F32_MERGE ? 2 : (o_dtype == LCB_DTYPE_F32 ? 1 : 0);
   a.scale = scale;
   int rc = dev_status(&a.st);
   if (rc != LCB_OK) return rc;

@@ -60,7 +60,7 @@ struct Params {
   void* o;
   float* lse;
   long long o_rs, o_bs, l_hs, l_bs;
-  int B, H, Sq, Sk, causal, o_f32;
+  int B, H, Sq, Sk, causal, o_mode;  // o_mode: 0 bf16 out, 1 fp32 out, 2 merge into fp32 (O, LSE)
   float scale_log2;
   DevStatus st;
 };
@@ -329,12 +329,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool valid = qi < p.Sq;
+      const long long lidx = b * p.l_bs + h * p.l_hs + qi;
+      const float lse_blk = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      // Merge mode (a fused ring step): O_acc <- (w_acc O_acc + w_blk O_blk) / (w_acc + w_blk)
+      // with w_x = exp(LSE_x - max); here O_blk = O_tmem / l, so its weight absorbs 1/l.
+      float c_acc = 0.f, c_blk = inv_l, lse_out = lse_blk;
+      if (p.o_mode == 2 && valid) {
+        const float la = p.lse[lidx];
+        const float mx = fmaxf(la, lse_blk);
+        if (mx == -INFINITY) {
+          c_blk = 0.f;
+          lse_out = -INFINITY;
+        } else {
+          const float wa = __expf(la - mx), wb = __expf(lse_blk - mx);
+          const float inv = 1.f / (wa + wb);
+          c_acc = wa * inv;
+          c_blk = wb * inv * inv_l;
+          lse_out = mx + __logf(wa + wb);
+        }
+      }
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t o[32];
         tmem_ld_x32(tO + ch * 32, o);
         if (valid) {
-          if (p.o_f32) {
+          if (p.o_mode == 2) {
+            float* dst = static_cast<float*>(p.o) + b * p.o_bs + static_cast<long long>(qi) * p.o_rs + h * kD + ch * 32;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              // an accumulator row with no keys yet (weight 0) is not read: its O may be unset
+              const float4 a = c_acc != 0.f ? *reinterpret_cast<const float4*>(dst + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+              float4 v = make_float4(c_acc * a.x + c_blk * __uint_as_float(o[i]),
+                                     c_acc * a.y + c_blk * __uint_as_float(o[i + 1]),
+                                     c_acc * a.z + c_blk * __uint_as_float(o[i + 2]),
+                                     c_acc * a.w + c_blk * __uint_as_float(o[i + 3]));
+              *reinterpret_cast<float4*>(dst + i) = v;
+            }
+          } else if (p.o_mode == 1) {
             float* dst = static_cast<float*>(p.o) + b * p.o_bs + static_cast<long long>(qi) * p.o_rs + h * kD + ch * 32;
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
@@ -357,10 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (valid) {
-        const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        p.lse[b * p.l_bs + h * p.l_hs + qi] = lse;
-      }
+      if (valid) p.lse[lidx] = lse_out;
     }
   }
 
@@ -418,7 +446,7 @@ int launch_attn_fwd(const FwdLaunch& a, cudaStream_t stream) {
   p.Sq = a.Sq;
   p.Sk = a.Sk;
   p.causal = a.causal;
-  p.o_f32 = a.o_f32;
+  p.o_mode = a.o_mode;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.st = a.st;
   const long long nq = (a.Sq + 2 * kBM - 1) / (2 * kBM);

@@ -28,7 +28,7 @@ struct FwdLaunch {
   float* lse;
   long long o_row_stride, o_batch_stride;
   long long lse_head_stride, lse_batch_stride;
-  int B, H, Sq, Sk, causal, o_f32;
+  int B, H, Sq, Sk, causal, o_mode;  // 0 bf16, 1 fp32, 2 merge into fp32 (O, LSE)
   float scale;
   DevStatus st;
 };

@@ -14,8 +14,9 @@ step 1, ...), as the real ring would run them in parallel. Every piece of
 arithmetic runs in libattn.so kernels:
 
   forward  step 0 (DIAG): attn_fwd_ex, causal, writing the fp32 accumulator
-           step s > 0   : attn_fwd_ex (non-causal block, bf16) then
-                          attn_lse_merge into the fp32 accumulator
+           step s > 0   : attn_fwd_ex in merge mode, folding the block into the
+                          fp32 accumulator in its epilogue (or, unfused, a
+                          bf16 block result then attn_lse_merge)
            end          : lcb_cast_f32_bf16 of the accumulator
   backward Delta from the final bf16 O (attn_bwd_preprocess), then per task
            attn_bwd_ex with the rank's FINAL merged LSE and Delta; fp32
@@ -55,10 +56,13 @@ class ZigzagPlan:
         return _lib.permute_rows(x, out, self.perm_dev, scatter=True)
 
 
-def zigzag_attention_fwd(qz, kz, vz, plan, scale=None, o_acc=None, lse=None, o_blk=None, lse_blk=None, o=None):
+def zigzag_attention_fwd(qz, kz, vz, plan, scale=None, o_acc=None, lse=None, o_blk=None, lse_blk=None, o=None,
+                         fused=True):
     """Forward of the emulated ring on zigzag-ordered [1, S, H, D] bf16 inputs.
 
     Returns (o bf16, lse fp32 [1, H, S], o_acc fp32), all in zigzag order.
+    fused=True merges each step inside the forward kernel's epilogue; False
+    writes the block result and runs the separate merge kernel.
     Buffers may be passed in to keep allocation out of a timed loop.
     """
     B, S, H, D = qz.shape
@@ -77,6 +81,8 @@ def zigzag_attention_fwd(qz, kz, vz, plan, scale=None, o_acc=None, lse=None, o_b
         ks = slice(t["k_off"], t["k_off"] + t["k_len"])
         if t["step"] == 0:
             _lib.attn_fwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], o_acc[:, qs], lse[:, :, qs], True, scale)
+        elif fused:
+            _lib.attn_fwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], o_acc[:, qs], lse[:, :, qs], False, scale, merge=True)
         else:
             n = t["q_len"]
             _lib.attn_fwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], o_blk[:, :n], lse_blk[:, :, :n], False, scale)

@@ -69,3 +69,67 @@ def test_config3_zigzag_131072_p8():
     assert_bf16_close(to64(r["oz"][:, zpos]), ref["o"], "O C3 sampled vs oracle")
     assert_lse_close(to64(r["lsez"][:, :, zpos]), ref["lse"])
     assert_bf16_close(to64(r["dqz"][:, zpos]), ref["dq"], "dQ C3 sampled vs oracle")
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_ring_forward_fused_and_unfused_agree(fused):
+    """Both forward step forms (merge in the kernel epilogue, or block result +
+    merge kernel) reproduce monolithic attention."""
+    S, H, P = 4096, 2, 4
+    q, k, v, _ = gaussian_qkvdo(1, H, S, D, seed=77)
+    plan = ZigzagPlan(S, P, "cuda")
+    qz, kz, vz = (plan.gather(x) for x in (q, k, v))
+    oz, lsez, _ = lcb.zigzag_attention_fwd(qz, kz, vz, plan, fused=fused)
+    o, lse = lcb.attn_fwd(q, k, v)
+    perm = torch.as_tensor(plan.perm, device="cuda", dtype=torch.long)
+    assert_bf16_close(to64(oz), to64(o[:, perm]), f"O zigzag fused={fused}")
+    assert_lse_close(to64(lsez), to64(lse[:, :, perm]))
+
+
+@pytest.mark.parametrize("Sq,Sk1,Sk2", [(384, 256, 384), (200, 130, 70)])
+def test_forward_merge_mode_vs_oracle(Sq, Sk1, Sk2):
+    """attn_fwd_ex in merge mode: the accumulator holds attention over keys
+    [0, Sk1); merging the block over keys [Sk1, Sk1 + Sk2) gives attention over
+    all keys (oracle, non-causal), and equals the unfused block + merge kernel."""
+    H = 3
+    g = torch.Generator().manual_seed(Sq + Sk1 + Sk2)
+    q, k, v = (torch.randn(1, n, H, D, generator=g).to("cuda", torch.bfloat16) for n in (Sq, Sk1 + Sk2, Sk1 + Sk2))
+    scale = D ** -0.5
+    k1, v1, k2, v2 = k[:, :Sk1], v[:, :Sk1], k[:, Sk1:], v[:, Sk1:]
+    acc = torch.empty(1, Sq, H, D, device="cuda", dtype=torch.float32)
+    lse = torch.empty(1, H, Sq, device="cuda", dtype=torch.float32)
+    lcb._lib.attn_fwd_ex(q, k1, v1, acc, lse, False, scale)
+    acc2, lse2 = acc.clone(), lse.clone()
+    lcb._lib.attn_fwd_ex(q, k2, v2, acc, lse, False, scale, merge=True)
+    ob = torch.empty(1, Sq, H, D, device="cuda", dtype=torch.bfloat16)
+    lb = torch.empty(1, H, Sq, device="cuda", dtype=torch.float32)
+    lcb._lib.attn_fwd_ex(q, k2, v2, ob, lb, False, scale)
+    lcb._lib.attn_lse_merge(acc2, lse2, ob, lb)
+    torch.cuda.synchronize()
+    ref_o, ref_lse = oracle.attn_fwd(to64(q), to64(k), to64(v), False, scale)
+    assert_bf16_close(to64(acc), ref_o, "O merge mode vs oracle")
+    assert_lse_close(to64(lse), ref_lse)
+    # the fused form keeps the block in fp32; the unfused one rounds it to bf16 first
+    assert_bf16_close(to64(acc), to64(acc2), "O merge mode vs unfused", max_abs=1e-2, mean_abs=1e-3)
+    assert_lse_close(to64(lse), to64(lse2), tol=1e-5)
+
+
+def test_forward_merge_mode_empty_sides():
+    """An accumulator row with LSE = -inf (no keys yet) takes the block's result
+    whatever its O holds; a block with no keys leaves the accumulator as it was."""
+    Sq, Sk, H = 160, 96, 2
+    g = torch.Generator().manual_seed(5)
+    q, k, v = (torch.randn(1, n, H, D, generator=g).to("cuda", torch.bfloat16) for n in (Sq, Sk, Sk))
+    scale = D ** -0.5
+    acc = torch.full((1, Sq, H, D), float("nan"), device="cuda")
+    lse = torch.full((1, H, Sq), float("-inf"), device="cuda")
+    lcb._lib.attn_fwd_ex(q, k, v, acc, lse, False, scale, merge=True)
+    torch.cuda.synchronize()
+    ref_o, ref_lse = oracle.attn_fwd(to64(q), to64(k), to64(v), False, scale)
+    assert torch.isfinite(acc).all()
+    assert_bf16_close(to64(acc), ref_o, "O merge into empty accumulator")
+    assert_lse_close(to64(lse), ref_lse)
+    before_o, before_l = acc.clone(), lse.clone()
+    lcb._lib.attn_fwd_ex(q, k[:, :0], v[:, :0], acc, lse, False, scale, merge=True)
+    torch.cuda.synchronize()
+    assert torch.equal(acc, before_o) and torch.equal(lse, before_l)
