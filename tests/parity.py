@@ -5,6 +5,9 @@ max-abs 2e-2 and mean-abs 2e-3 of the fp64 oracle; LSE within 1e-3
 absolute; schedule and index work bit-exact.
 """
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 MAX_ABS = 2e-2
@@ -43,3 +46,23 @@ def assert_lse_close(got, want, name="lse", tol=LSE_ABS):
         assert mx <= tol, f"{name}: max-abs {mx:.3e} (bar {tol})"
         return mx
     return 0.0
+
+
+def rows_budget(default):
+    """Sampled rows per head for the large-size parity tests (LCB_PARITY_ROWS
+    raises or lowers it)."""
+    return int(os.environ.get("LCB_PARITY_ROWS", default))
+
+
+def head64(t, h):
+    """One head of a [B, S, H, D] device tensor as fp64 numpy [B, S, 1, D]."""
+    return t[:, :, h:h + 1].float().cpu().numpy().astype(np.float64)
+
+
+def map_heads(fn, heads, workers=None):
+    """fn(h) for every head on a thread pool. numpy's BLAS calls and large
+    ufunc loops release the GIL, so the per-head oracle calls overlap; the
+    oracle itself is unchanged."""
+    workers = workers or min(8, os.cpu_count() or 1)
+    with ThreadPoolExecutor(max_workers=max(1, min(workers, len(heads)))) as ex:
+        return list(ex.map(fn, heads))

@@ -7,7 +7,7 @@ import torch
 import oracle
 import long_context_causal_blockwise_gb300 as lcb
 from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo, sample_rows
-from parity import assert_bf16_close, to64
+from parity import assert_bf16_close, assert_lse_close, head64, map_heads, rows_budget, to64
 
 pytestmark = pytest.mark.gpu
 D = 128
@@ -106,22 +106,30 @@ def test_empty_sides():
 
 
 def test_config2_sampled_rows_backward():
-    """B=1, H=32, S=32768: dQ on sampled query rows of every head; dK/dV on
-    sampled key rows of two heads; the sum invariants on every head."""
+    """B=1, H=32, S=32768: O, LSE and dQ on 4096 sampled query rows of every
+    head; dK/dV on 4096 sampled key rows of two heads; the sum invariants on
+    every head."""
     B, H, S = 1, 32, 32768
+    scale = D ** -0.5
     q, k, v, do = gaussian_qkvdo(B, H, S, D, seed=0)
     o, lse = lcb.attn_fwd(q, k, v)
     dq, dk, dv = lcb.attn_bwd(q, k, v, o, lse, do)
     torch.cuda.synchronize()
-    rows = sample_rows(S, 128, seed=1)
-    q64, k64, v64, do64 = to64(q), to64(k), to64(v), to64(do)
-    ref = oracle.attn_rows(q64, k64, v64, do64, rows, True, D ** -0.5)
-    assert_bf16_close(to64(dq[:, rows]), ref["dq"], "dQ C2 sampled")
-    keys = sample_rows(S, 128, seed=2)
+    rows = sample_rows(S, rows_budget(4096), seed=1)
+    refs = map_heads(lambda h: oracle.attn_rows(*(head64(t, h) for t in (q, k, v, do)), rows, True, scale),
+                     list(range(H)))
+    rows_d = torch.as_tensor(rows, device="cuda")
+    assert_bf16_close(to64(o[:, rows_d]), np.concatenate([r["o"] for r in refs], 2), "O C2 sampled")
+    assert_lse_close(to64(lse[:, :, rows_d]), np.concatenate([r["lse"] for r in refs], 1))
+    assert_bf16_close(to64(dq[:, rows_d]), np.concatenate([r["dq"] for r in refs], 2), "dQ C2 sampled")
+    keys = sample_rows(S, rows_budget(4096), seed=2)
+    keys_d = torch.as_tensor(keys, device="cuda")
     heads = [0, 31]
-    rdk, rdv = oracle.attn_key_rows(q64, k64, v64, do64, keys, heads, True, D ** -0.5)
-    assert_bf16_close(to64(dk[:, keys][:, :, heads]), rdk, "dK C2 sampled")
-    assert_bf16_close(to64(dv[:, keys][:, :, heads]), rdv, "dV C2 sampled")
+    kref = map_heads(lambda h: oracle.attn_key_rows(*(head64(t, h) for t in (q, k, v, do)), keys, [0], True, scale),
+                     heads)
+    for h, (rdk, rdv) in zip(heads, kref):
+        assert_bf16_close(to64(dk[:, keys_d, h:h + 1]), rdk, f"dK C2 sampled head {h}")
+        assert_bf16_close(to64(dv[:, keys_d, h:h + 1]), rdv, f"dV C2 sampled head {h}")
     # sum_j dV_j = sum_i dO_i and sum_j dK_j = 0, per head (fp32 sums of bf16 values)
     sdv = dv.float().sum(1)
     sdo = do.float().sum(1)

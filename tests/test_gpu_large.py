@@ -4,11 +4,12 @@
   * Long-context stress: B=1, H=32, D=128, S=524288, causal, Q and K
     pre-rotated by RoPE with theta = 1e6 over positions 0..S-1.
 
-Checked against the fp64 oracle: O, LSE and dQ on sampled query rows of every
-head (row-local); dK and dV on the last keys of the sequence for two heads
-(under the causal mask only the final queries see them, so the oracle forms
-just those rows in full); and the sum rules sum_j dV_j = sum_i dO_i and
-sum_j dK_j = 0 on every head, which hold at any size.
+Checked against the fp64 oracle: O, LSE and dQ on 1024 sampled query rows of
+every head (row-local; LCB_PARITY_ROWS changes the count); dK and dV on the
+last keys of the sequence for two heads (under the causal mask only the final
+queries see them, so the oracle forms just those rows in full); and the sum
+rules sum_j dV_j = sum_i dO_i and sum_j dK_j = 0 on every head, which hold at
+any size.
 """
 
 import numpy as np
@@ -18,18 +19,14 @@ import torch
 import oracle
 import long_context_causal_blockwise_gb300 as lcb
 from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo, sample_rows
-from parity import assert_bf16_close, assert_lse_close, to64
+from parity import assert_bf16_close, assert_lse_close, head64, map_heads, rows_budget, to64
 
 pytestmark = pytest.mark.gpu
 D = 128
 
 
-def _h64(t, h):
-    """One head of a [B, S, H, D] device tensor as fp64 numpy [B, S, 1, D]."""
-    return t[:, :, h:h + 1].float().cpu().numpy().astype(np.float64)
-
-
 def _check_large(H, S, rope_theta, seed, n_rows, tail):
+    scale = D ** -0.5
     q, k, v, do = gaussian_qkvdo(1, H, S, D, seed=seed, rope_theta=rope_theta)
     o, lse = lcb.attn_fwd(q, k, v)
     dq, dk, dv = lcb.attn_bwd(q, k, v, o, lse, do)
@@ -40,32 +37,30 @@ def _check_large(H, S, rope_theta, seed, n_rows, tail):
     rows_d = torch.as_tensor(rows, device="cuda")
     keys = np.arange(S - tail, S)
     keys_d = torch.as_tensor(keys, device="cuda")
-    got = {"o": [], "lse": [], "dq": []}
-    want = {"o": [], "lse": [], "dq": []}
-    for h in range(H):  # one head at a time keeps the fp64 copies small
-        q64, k64, v64, do64 = (_h64(t, h) for t in (q, k, v, do))
-        ref = oracle.attn_rows(q64, k64, v64, do64, rows, True, D ** -0.5)
-        want["o"].append(ref["o"])
-        want["lse"].append(ref["lse"])
-        want["dq"].append(ref["dq"])
-        got["o"].append(to64(o[:, rows_d, h:h + 1]))
-        got["lse"].append(to64(lse[:, h:h + 1, rows_d]))
-        got["dq"].append(to64(dq[:, rows_d, h:h + 1]))
+
+    def one_head(h):  # one head per call keeps the fp64 copies small
+        q64, k64, v64, do64 = (head64(t, h) for t in (q, k, v, do))
+        ref = oracle.attn_rows(q64, k64, v64, do64, rows, True, scale)
         if h in (0, H - 1):
-            rdk, rdv = oracle.attn_key_rows(q64, k64, v64, do64, keys, [0], True, D ** -0.5)
-            assert_bf16_close(to64(dk[:, keys_d, h:h + 1]), rdk, f"dK tail keys S{S} head {h}")
-            assert_bf16_close(to64(dv[:, keys_d, h:h + 1]), rdv, f"dV tail keys S{S} head {h}")
-    assert_bf16_close(np.concatenate(got["o"], 2), np.concatenate(want["o"], 2), f"O sampled S{S}")
-    assert_lse_close(np.concatenate(got["lse"], 1), np.concatenate(want["lse"], 1))
-    assert_bf16_close(np.concatenate(got["dq"], 2), np.concatenate(want["dq"], 2), f"dQ sampled S{S}")
+            ref["keys"] = oracle.attn_key_rows(q64, k64, v64, do64, keys, [0], True, scale)
+        return ref
+
+    refs = map_heads(one_head, list(range(H)))
+    for h in (0, H - 1):
+        rdk, rdv = refs[h]["keys"]
+        assert_bf16_close(to64(dk[:, keys_d, h:h + 1]), rdk, f"dK tail keys S{S} head {h}")
+        assert_bf16_close(to64(dv[:, keys_d, h:h + 1]), rdv, f"dV tail keys S{S} head {h}")
+    assert_bf16_close(to64(o[:, rows_d]), np.concatenate([r["o"] for r in refs], 2), f"O sampled S{S}")
+    assert_lse_close(to64(lse[:, :, rows_d]), np.concatenate([r["lse"] for r in refs], 1))
+    assert_bf16_close(to64(dq[:, rows_d]), np.concatenate([r["dq"] for r in refs], 2), f"dQ sampled S{S}")
     sdv, sdo, sdk = dv.float().sum(1), do.float().sum(1), dk.float().sum(1)
     assert ((sdv - sdo).norm(dim=-1) <= 1e-2 * sdo.norm(dim=-1)).all()
     assert (sdk.norm(dim=-1) <= 1e-2 * dk.float().norm(dim=(1, 3))).all()
 
 
 def test_config4_llama13b_layer_262144():
-    _check_large(H=40, S=262144, rope_theta=None, seed=4, n_rows=24, tail=96)
+    _check_large(H=40, S=262144, rope_theta=None, seed=4, n_rows=rows_budget(1024), tail=96)
 
 
 def test_config5_stress_524288_rope():
-    _check_large(H=32, S=524288, rope_theta=1e6, seed=5, n_rows=16, tail=64)
+    _check_large(H=32, S=524288, rope_theta=1e6, seed=5, n_rows=rows_budget(1024), tail=64)

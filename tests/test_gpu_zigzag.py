@@ -12,7 +12,7 @@ import oracle
 import long_context_causal_blockwise_gb300 as lcb
 from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo, sample_rows
 from long_context_causal_blockwise_gb300.zigzag import ZigzagPlan
-from parity import assert_bf16_close, assert_lse_close, to64
+from parity import assert_bf16_close, assert_lse_close, head64, map_heads, rows_budget, to64
 
 pytestmark = pytest.mark.gpu
 D = 128
@@ -55,20 +55,24 @@ def test_small_zigzag_vs_monolithic_and_oracle(S, H, P):
 
 def test_config3_zigzag_131072_p8():
     """B=1, H=32, S=131072, P=8 (16 chunks of 8192): ring result vs monolithic
-    on every element, and vs the oracle on sampled query rows."""
+    on every element, and vs the oracle on 512 sampled query rows plus every
+    chunk edge, on every head."""
     S, H, P = 131072, 32, 8
     r = _run(S, H, P, seed=0)
     _vs_monolithic(r, "C3")
-    rows = sample_rows(S, 48, seed=3)
-    # chunk edges of the zigzag split are among the most likely places to go wrong
+    rows = sample_rows(S, rows_budget(512), seed=3)
+    # every chunk edge of the zigzag split: among the most likely places to go wrong
     c = S // (2 * P)
-    rows = np.unique(np.concatenate([rows, [c - 1, c, 7 * c - 1, 7 * c, 8 * c, 15 * c - 1]]))
-    ref = oracle.attn_rows(to64(r["q"]), to64(r["k"]), to64(r["v"]), to64(r["do"]), rows, True, D ** -0.5)
+    edges = [e for j in range(1, 2 * P) for e in (j * c - 1, j * c)]
+    rows = np.unique(np.concatenate([rows, edges]))
+    refs = map_heads(lambda h: oracle.attn_rows(*(head64(r[n], h) for n in ("q", "k", "v", "do")), rows, True,
+                                                D ** -0.5), list(range(H)))
     inv = np.argsort(np.asarray(r["plan"].perm))
     zpos = torch.as_tensor(inv[rows], device="cuda")
-    assert_bf16_close(to64(r["oz"][:, zpos]), ref["o"], "O C3 sampled vs oracle")
-    assert_lse_close(to64(r["lsez"][:, :, zpos]), ref["lse"])
-    assert_bf16_close(to64(r["dqz"][:, zpos]), ref["dq"], "dQ C3 sampled vs oracle")
+    assert_bf16_close(to64(r["oz"][:, zpos]), np.concatenate([x["o"] for x in refs], 2), "O C3 sampled vs oracle")
+    assert_lse_close(to64(r["lsez"][:, :, zpos]), np.concatenate([x["lse"] for x in refs], 1))
+    assert_bf16_close(to64(r["dqz"][:, zpos]), np.concatenate([x["dq"] for x in refs], 2),
+                      "dQ C3 sampled vs oracle")
 
 
 @pytest.mark.parametrize("fused", [True, False])
