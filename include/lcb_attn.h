@@ -111,14 +111,20 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
                 long long o_batch_stride, int o_dtype, long long lse_head_stride, long long lse_batch_stride,
                 void* stream);
 
-/* Bytes of device workspace attn_bwd needs (Delta, fp32 [B,H,S]). */
+/* Bytes of device workspace attn_bwd needs: Delta (fp32 [B,H,S]) and the
+ * fused pass's tiled fp32 dQ accumulator (B*H*ceil(S/128) tiles of 128x128);
+ * 0 for D != 128. */
 size_t attn_bwd_workspace_bytes(int B, int H, int S, int D);
 
 /*
  * attn_bwd — backward of attn_fwd with recomputation, [FA] §2 ("重新计算").
  * Inputs q, k, v, o, dO bf16 [B,S,H,D] and lse fp32 [B,H,S] as returned by
  * attn_fwd; outputs dq, dk, dv bf16 [B,S,H,D] (overwritten). Runs the
- * Delta = rowsum(dO * O) preprocess, then a dK/dV pass and a dQ pass.
+ * Delta = rowsum(dO * O) preprocess, zeroes the tiled fp32 dQ accumulator in
+ * the workspace, runs the fused pass (attn_bwd_fused_ex) and converts dQ to
+ * bf16 (lcb_dq_untile).
+ * dQ's fp32 summation order is not fixed (atomic adds), so repeated calls may
+ * differ in the last bits of dq; dk and dv are deterministic.
  * workspace: device memory of at least attn_bwd_workspace_bytes(), 16-byte
  * aligned, owned by the caller, contents ignored.
  */
@@ -155,6 +161,45 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const float* lse, c
                 long long kv_batch_stride, long long lse_head_stride, long long lse_batch_stride, int grad_mode,
                 long long dq_row_stride, long long dq_batch_stride, long long dkv_row_stride,
                 long long dkv_batch_stride, void* stream);
+
+/*
+ * attn_bwd_fused_ex — attn_bwd_ex's gradients in ONE pass over the (key tile,
+ * query tile) pairs, [FA] §2: each CTA owns 128 keys, keeps dK and dV in
+ * TMEM, and adds every query tile's partial dQ = scale * dS K into a TILED
+ * fp32 accumulator with bulk asynchronous reductions. Five tensor-core
+ * products per tile pair instead of the two passes' seven (dQ's S and dP are
+ * not recomputed). dQ's summation order is not fixed.
+ * dq_tiles: fp32, the tile holding this call's query rows [128t, 128t+128) of
+ *   (b, h) starts at dq_tiles + b*dq_tile_batch_stride + h*dq_tile_head_stride
+ *   + t*16384 (floats; 16-byte aligned; strides multiples of 4). Inside a
+ *   tile, block x = 0..3 (columns [32x, 32x+32)) is at x*4096, row r of the
+ *   block at r*32, and its four-float chunk c (columns 32x+4c..) at chunk
+ *   position c ^ (r & 7). ALWAYS added into: zero it for a fresh gradient;
+ *   lcb_dq_untile converts it to bf16 rows. A ring whose query blocks start
+ *   at multiples of 128 rows accumulates all its steps into one such buffer.
+ * grad_mode applies to dk and dv only (LCB_GRAD_BF16: bf16 overwritten;
+ *   LCB_GRAD_F32_ACCUM / _STORE: fp32 added into / overwritten).
+ * Other arguments and errors as attn_bwd_ex.
+ */
+int attn_bwd_fused_ex(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                      const void* dO, float* dq_tiles, void* dk, void* dv, int B, int H, int Sq, int Sk, int D,
+                      int causal, float scale, long long q_row_stride, long long q_batch_stride,
+                      long long kv_row_stride, long long kv_batch_stride, long long lse_head_stride,
+                      long long lse_batch_stride, int grad_mode, long long dq_tile_head_stride,
+                      long long dq_tile_batch_stride, long long dkv_row_stride, long long dkv_batch_stride,
+                      void* stream);
+
+/* lcb_dq_tiles_zero — zeroes n_floats of a tiled dQ accumulator (an async
+ * memset on `stream`; dq_tiles 16-byte aligned). */
+int lcb_dq_tiles_zero(float* dq_tiles, long long n_floats, void* stream);
+
+/*
+ * lcb_dq_untile — the tiled fp32 dQ accumulator of attn_bwd_fused_ex (tile
+ * strides as there) to bf16 rows of a [B, S, H, D] view (row/batch strides in
+ * elements, dq 8-byte aligned): dq[b, s, h, :] = tile rows as stored.
+ */
+int lcb_dq_untile(const float* dq_tiles, long long tile_head_stride, long long tile_batch_stride, void* dq,
+                  long long row_stride, long long batch_stride, int B, int H, int S, void* stream);
 
 /*
  * attn_bwd_dkdv_ex / attn_bwd_dq_ex — the two passes of attn_bwd_ex on their

@@ -56,6 +56,10 @@ _SIGNATURES = {
     "attn_bwd_preprocess": ([_P, _P, _P, _I, _I, _I, _I, _LL, _LL, _LL, _LL, _P], _I),
     "attn_bwd_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _I,
                      _LL, _LL, _LL, _LL, _P], _I),
+    "attn_bwd_fused_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL,
+                           _LL, _I, _LL, _LL, _LL, _LL, _P], _I),
+    "lcb_dq_tiles_zero": ([_P, _LL, _P], _I),
+    "lcb_dq_untile": ([_P, _LL, _LL, _P, _LL, _LL, _I, _I, _I, _P], _I),
     "attn_bwd_dkdv_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL,
                           _I, _LL, _LL, _LL, _LL, _P], _I),
     "attn_bwd_dq_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _I,
@@ -248,7 +252,12 @@ def attn_bwd_ex(q, k, v, lse, delta, do, dq, dk, dv, causal, scale, accumulate=T
     """Block backward with given row statistics.
 
     bf16 gradients are overwritten; fp32 gradients are accumulated into
-    (accumulate=True) or overwritten (accumulate=False)."""
+    (accumulate=True) or overwritten (accumulate=False).
+    passes: "both" (the deterministic two-pass form), "dkdv" or "dq" (one of
+    its passes), or "fused" (one pass; dq is then a tiled fp32 accumulator
+    [B, H, T, 16384] from dq_tiles_zeros, or a slice of one along T starting
+    at this call's first query tile, always added into; dk/dv follow their
+    dtype and `accumulate`)."""
     B, Sq, H, D = q.shape
     Sk = k.shape[1]
     qr, qb = _bshd(q, "q")
@@ -260,22 +269,57 @@ def attn_bwd_ex(q, k, v, lse, delta, do, dq, dk, dv, causal, scale, accumulate=T
     lh, lb = _bhs(lse, "lse")
     if _bhs(delta, "delta") != (lh, lb):
         raise ValueError("lse and delta must share strides")
-    gdt = dq.dtype
-    if dk.dtype != gdt or dv.dtype != gdt:
+    gdt = dk.dtype
+    if dv.dtype != gdt:
+        raise ValueError("dk and dv must share a dtype")
+    if passes == "fused":
+        if dq.dtype != torch.float32 or dq.dim() != 4 or dq.shape[3] != 128 * 128 or dq.stride(3) != 1 \
+                or dq.stride(2) != 128 * 128 or dq.shape[0] != B or dq.shape[1] != H or dq.shape[2] * 128 < Sq:
+            raise ValueError("the fused pass adds dQ into a tiled fp32 accumulator (dq_tiles_zeros)")
+    elif dq.dtype != gdt:
         raise ValueError("dq, dk, dv must share a dtype")
     if gdt == torch.float32:
         grad_mode = LCB_GRAD_F32_ACCUM if accumulate else LCB_GRAD_F32_STORE
     else:
         grad_mode = LCB_GRAD_BF16
-    dqr, dqb = _bshd(dq, "dq", gdt)
+    if passes == "fused":
+        dqr, dqb = dq.stride(1), dq.stride(0)  # tile head and batch strides
+    else:
+        dqr, dqb = _bshd(dq, "dq", dq.dtype)
     dkr, dkb = _bshd(dk, "dk", gdt)
     if _bshd(dv, "dv", gdt) != (dkr, dkb):
         raise ValueError("dk and dv must share strides")
-    fname = {"both": "attn_bwd_ex", "dkdv": "attn_bwd_dkdv_ex", "dq": "attn_bwd_dq_ex"}[passes]
+    fname = {"both": "attn_bwd_ex", "dkdv": "attn_bwd_dkdv_ex", "dq": "attn_bwd_dq_ex",
+             "fused": "attn_bwd_fused_ex"}[passes]
     _check(fname, getattr(load(), fname)(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(do), _ptr(dq),
                                              _ptr(dk), _ptr(dv), B, H, Sq, Sk, D, int(causal), float(scale), qr, qb,
                                              kr, kb, lh, lb, grad_mode, dqr, dqb, dkr, dkb, _stream(q)))
     return dq, dk, dv
+
+
+def dq_tiles_zeros(B, H, S, device):
+    """A zeroed tiled fp32 dQ accumulator for the fused pass: [B, H, ceil(S/128), 128*128]."""
+    return torch.zeros((B, H, (S + 127) // 128, 128 * 128), dtype=torch.float32, device=device)
+
+
+def dq_tiles_zero_(tiles):
+    """Zeroes a tiled dQ accumulator in place (on the current stream); returns it."""
+    if tiles.dtype != torch.float32 or not tiles.is_contiguous():
+        raise ValueError("tiles must be a contiguous fp32 accumulator (dq_tiles_zeros)")
+    _check("lcb_dq_tiles_zero", load().lcb_dq_tiles_zero(_ptr(tiles), tiles.numel(), _stream(tiles)))
+    return tiles
+
+
+def dq_untile(tiles, dq):
+    """Tiled fp32 accumulator -> bf16 rows of dq ([B, S, H, D] view); returns dq."""
+    B, S, H, D = dq.shape
+    r, b = _bshd(dq, "dq")
+    if tiles.dtype != torch.float32 or tiles.dim() != 4 or tiles.shape[:2] != (B, H) or tiles.shape[2] * 128 < S \
+            or tiles.stride(3) != 1 or tiles.stride(2) != 128 * 128:
+        raise ValueError("tiles must be a tiled fp32 accumulator covering dq (dq_tiles_zeros)")
+    _check("lcb_dq_untile", load().lcb_dq_untile(_ptr(tiles), tiles.stride(1), tiles.stride(0), _ptr(dq), r, b, B, H,
+                                                 S, _stream(dq)))
+    return dq
 
 
 # ------------------------------------------------------------------ merge / zigzag

@@ -216,11 +216,19 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
                      static_cast<long long>(H) * S, stream);
 }
 
-size_t attn_bwd_workspace_bytes(int B, int H, int S, int D) {
-  (void)D;
-  if (B < 1 || H < 1 || S < 0) return 0;
+// Workspace of attn_bwd: Delta [B, H, S] fp32, then the fused pass's tiled
+// fp32 dQ accumulator (B * H * ceil(S / 128) tiles of 128 x 128), each at a
+// 256-byte boundary.
+static size_t delta_bytes(int B, int H, int S) {
   const size_t n = static_cast<size_t>(B) * H * S * sizeof(float);
   return (n + 255) & ~static_cast<size_t>(255);
+}
+static long long dq_tiles(int S) { return (S + 127) / 128; }
+constexpr long long kDqTileFloats = 128LL * 128;
+
+size_t attn_bwd_workspace_bytes(int B, int H, int S, int D) {
+  if (B < 1 || H < 1 || S < 0 || D != kHeadDim) return 0;
+  return delta_bytes(B, H, S) + static_cast<size_t>(B) * H * dq_tiles(S) * kDqTileFloats * sizeof(float);
 }
 
 int attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H, int S, int D,
@@ -322,6 +330,55 @@ int attn_bwd_dq_ex(const void* q, const void* k, const void* v, const float* lse
   return finish(launch_attn_bwd_dq(a, st), st);
 }
 
+int attn_bwd_fused_ex(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                      const void* dO, float* dq_tiles, void* dk, void* dv, int B, int H, int Sq, int Sk, int D,
+                      int causal, float scale, long long q_row_stride, long long q_batch_stride,
+                      long long kv_row_stride, long long kv_batch_stride, long long lse_head_stride,
+                      long long lse_batch_stride, int grad_mode, long long dq_tile_head_stride,
+                      long long dq_tile_batch_stride, long long dkv_row_stride, long long dkv_batch_stride,
+                      void* stream) {
+  // The accumulator is checked here; prep_bwd sees row strides that always pass.
+  if (dq_tile_head_stride < 0 || dq_tile_batch_stride < 0 || (dq_tile_head_stride % 4) ||
+      (dq_tile_batch_stride % 4))
+    return LCB_ERR_ARG;
+  void* dq = dq_tiles;
+  const long long HD = static_cast<long long>(H) * kHeadDim;
+  const long long dq_row_stride = HD, dq_batch_stride = HD * Sq;
+  BwdLaunch a;
+  int rc = prep_bwd(&a, LCB_BWD_EX_ARGS);
+  if (rc != LCB_OK) return rc;
+  a.dq_row_stride = dq_tile_head_stride;
+  a.dq_batch_stride = dq_tile_batch_stride;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return finish(launch_attn_bwd_fused(a, st), st);
+}
+
+int lcb_dq_tiles_zero(float* dq_tiles, long long n_floats, void* stream) {
+  if (n_floats < 0) return LCB_ERR_ARG;
+  if (n_floats == 0) return LCB_OK;
+  if (!dq_tiles || !aligned16(dq_tiles)) return LCB_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(dq_tiles, 0, static_cast<size_t>(n_floats) * sizeof(float), st) != cudaSuccess)
+    return LCB_ERR_CUDA;
+  return finish(LCB_OK, st);
+}
+
+int lcb_dq_untile(const float* dq_tiles, long long tile_head_stride, long long tile_batch_stride, void* dq,
+                  long long row_stride, long long batch_stride, int B, int H, int S, void* stream) {
+  if (B < 1 || H < 1 || S < 0) return LCB_ERR_ARG;
+  if (S == 0) return LCB_OK;
+  if (!dq_tiles || !dq || !aligned16(dq_tiles) || (reinterpret_cast<uintptr_t>(dq) & 7u)) return LCB_ERR_ARG;
+  if (tile_head_stride < 0 || tile_batch_stride < 0 || (tile_head_stride % 4) || (tile_batch_stride % 4))
+    return LCB_ERR_ARG;
+  if (row_stride < static_cast<long long>(H) * kHeadDim || (row_stride % 4) || batch_stride < 0 ||
+      (batch_stride % 4))
+    return LCB_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return finish(launch_dq_untile(dq_tiles, tile_head_stride, tile_batch_stride, dq, row_stride, batch_stride, B, H,
+                                 S, st),
+                st);
+}
+
 int attn_bwd_ex(const void* q, const void* k, const void* v, const float* lse, const float* delta,
                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, int causal,
                 float scale, long long q_row_stride, long long q_batch_stride, long long kv_row_stride,
@@ -344,13 +401,20 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
   if (S == 0) return LCB_OK;
   if (!workspace || !aligned16(workspace) || ws_bytes < attn_bwd_workspace_bytes(B, H, S, D)) return LCB_ERR_ARG;
+  if (!dq || !aligned16(dq)) return LCB_ERR_ARG;
   const long long rs = static_cast<long long>(H) * D;
   const long long bs = rs * S;
   float* delta = static_cast<float*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes(B, H, S));
+  const long long tile_hs = dq_tiles(S) * kDqTileFloats, tile_bs = tile_hs * H;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = attn_bwd_preprocess(o, dO, delta, B, H, S, D, rs, bs, S, static_cast<long long>(H) * S, stream);
   if (rc != LCB_OK) return rc;
-  return attn_bwd_ex(q, k, v, lse, delta, dO, dq, dk, dv, B, H, S, S, D, causal, scale, rs, bs, rs, bs, S,
-                     static_cast<long long>(H) * S, LCB_GRAD_BF16, rs, bs, rs, bs, stream);
+  if ((rc = lcb_dq_tiles_zero(dq_acc, tile_bs * B, stream)) != LCB_OK) return rc;
+  rc = attn_bwd_fused_ex(q, k, v, lse, delta, dO, dq_acc, dk, dv, B, H, S, S, D, causal, scale, rs, bs, rs, bs, S,
+                         static_cast<long long>(H) * S, LCB_GRAD_BF16, tile_hs, tile_bs, rs, bs, stream);
+  if (rc != LCB_OK) return rc;
+  return lcb_dq_untile(dq_acc, tile_hs, tile_bs, dq, rs, bs, B, H, S, stream);
 }
 
 int attn_lse_merge(float* o_acc, float* lse_acc, const void* o_b, const float* lse_b, int o_b_dtype,

@@ -58,6 +58,10 @@ struct Bars {
   uint64_t pt_full;   // dK/dV pass: P^T written to TMEM
   uint64_t ds_free;   // the MMA that read dS from shared memory completed
   uint64_t acc_full;
+  uint64_t dq_full;   // fused pass: the dQ partial of one query tile is in TMEM
+  uint64_t dq_free;   // fused pass: it was loaded by every compute thread
+  uint64_t stg_full[4];  // fused pass: warpgroup x's dQ block is staged
+  uint64_t stg_free[4];  // fused pass: warpgroup x's staged block was read by the reducer
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -70,9 +74,11 @@ struct Params {
   const __nv_bfloat16* f0;  // dQ pass: Q and dO, written into TMEM as A operands
   const __nv_bfloat16* f1;
   long long f_rs, f_bs;
-  void* g0;  // dK (dK/dV pass) or dQ (dQ pass)
-  void* g1;  // dV (dK/dV pass)
+  void* g0;  // dK (dK/dV and fused passes) or dQ (dQ pass)
+  void* g1;  // dV (dK/dV and fused passes)
   long long g_rs, g_bs;
+  float* dq_acc;  // fused pass: tiled fp32 dQ accumulator, added into
+  long long dq_hs, dq_bs;  // its head and batch strides (floats)
   int B, H, Sq, Sk, causal, grad_mode;
   float scale, scale_log2;
   DevStatus st;
@@ -99,6 +105,8 @@ __device__ __forceinline__ void init_bars(Bars* bars, int stages, uint32_t fixed
   mbar_init(&bars->pt_full, kCompute);
   mbar_init(&bars->ds_free, 1);
   mbar_init(&bars->acc_full, 1);
+  mbar_init(&bars->dq_full, 1);
+  mbar_init(&bars->dq_free, kCompute);
   mbar_init(&bars->mma_done, 1);
   for (int s = 0; s < 2; ++s) {
     mbar_init(&bars->do_full[s], 1);
@@ -191,6 +199,15 @@ __device__ __forceinline__ void mma_ss_tile_mn(uint32_t d, uint32_t a, uint32_t 
     const uint32_t a_off = (kk >> 2) * kColHalf + (kk & 3) * 32;
     mma_ss(d, sdesc_sw128(a + a_off, 16, 1024), sdesc_sw128(b + kk * 2048, kColHalf, 1024), idesc,
            (accumulate || kk > 0));
+  }
+}
+
+// D = A x B over K = 128, A and B MN-major tiles [K rows][M or N = 128] (A^T and B as stored).
+__device__ __forceinline__ void mma_ss_tile_mnmn(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    mma_ss(d, sdesc_sw128(a + kk * 2048, kColHalf, 1024), sdesc_sw128(b + kk * 2048, kColHalf, 1024), idesc,
+           kk > 0);
   }
 }
 
@@ -527,6 +544,358 @@ __global__ void __launch_bounds__(kThreads, 1)
   teardown(tbase, warp);
 }
 
+// ============================================================== fused pass
+// One pass over the same (key tile, query tile) pairs as the dK/dV pass that
+// also forms dQ: per pair, dQ_i += scale dS_i K_j is one more MMA (A = dS read
+// MN-major from the dS^T tile, B = K read MN-major). Five MMAs per pair
+// instead of the seven of the two passes (dQ's S and dP are not recomputed).
+// The 128 x 128 fp32 partial of each pair is added into a tiled fp32 dQ
+// accumulator by bulk asynchronous reductions (whole 16 KB blocks, full
+// cache lines), not by per-thread atomics; its summation order is not fixed.
+//
+// Accumulator layout (floats): the tile of query rows [128t, 128t + 128) of
+// (b, h) is at dq + b * tile_bs + h * tile_hs + t * 16384, made of 4 blocks of
+// 4096 (columns [32x, 32x + 32)); row r of block x holds its 8 four-float
+// chunks c at chunk position c ^ (r & 7) (128 B per row).
+//
+// TMEM as in the dK/dV pass; the dQ partial of query tile i reuses the dP^T
+// columns once dP^T(i) is in registers. Shared memory: K, V, a 2-slot Q ring,
+// ONE dO slot (dO(i+1) loads while dS(i) is formed), dS^T, and two 16 KB
+// staging slots for dQ blocks (warpgroups x and x + 2 share slot x & 1).
+// Warps 0-15 compute, 16 TMA producer, 17 MMA issuer, 18 dQ reducer.
+// MMA order per query tile i: dV += P^T dO_i, S^T(i+1), dQ(i),
+// dK += dS^T Q_i, then dP^T(i+1) once dQ(i) has been read out.
+constexpr int kFuThreads = 608;
+constexpr int kFuReduceWarp = 18;
+constexpr uint32_t kDqBlock = 128 * 32 * 4;  // one staged dQ block: 128 rows x 32 columns fp32
+constexpr uint32_t kFuSmK = 0;
+constexpr uint32_t kFuSmV = kTileBytes;
+constexpr uint32_t kFuSmQ = 2 * kTileBytes;
+constexpr uint32_t kFuSmDo = kFuSmQ + kKvStages * kTileBytes;
+constexpr uint32_t kFuSmDs = kFuSmDo + kTileBytes;
+constexpr uint32_t kFuSmStg = kFuSmDs + kTileBytes;
+constexpr uint32_t kFuSmBar = kFuSmStg + 2 * kDqBlock;
+constexpr uint32_t kFuSmem = kFuSmBar + sizeof(Bars) + 1024;
+
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kFuThreads, 1)
+    attn_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                          const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kFuSmBar);
+  volatile int* abort_flag = &bars->abort;
+  const int warp = static_cast<int>(warp_id());
+  const int lane = static_cast<int>(lane_id());
+  constexpr uint32_t kWhere = 4u << 24;
+
+  // Work item and order as in the dK/dV pass (head-major, long rows first).
+  const int nq = (p.Sq + kT - 1) / kT;
+  const int nkt = (p.Sk + kT - 1) / kT;
+  const int bh = static_cast<int>(blockIdx.x / nkt);
+  const int kt = static_cast<int>(blockIdx.x % nkt);
+  const int b = bh / p.H, h = bh % p.H;
+  const int i0 = p.causal ? kt : 0;
+  const int n = std::max(0, nq - i0);  // query tiles
+
+  if (threadIdx.x == 0) {
+    for (int x = 0; x < 4; ++x) {
+      mbar_init(&bars->stg_full[x], 128);
+      mbar_init(&bars->stg_free[x], 1);
+    }
+  }
+  const uint32_t tbase = start(bars, kKvStages, 1, warp);  // its barrier fence covers the inits above
+  const uint32_t tS = tbase, tDP = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
+  const uint32_t tDQ = tDP;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      const int x0 = h * kD;
+      const uint64_t pol = l2_policy_evict_last();
+      mbar_arrive_expect_tx(&bars->fixed_full, 2 * kTileBytes);
+      load_tile(smem + kFuSmK, &tm_k, &bars->fixed_full, x0, kt * kT, b, pol);
+      load_tile(smem + kFuSmV, &tm_v, &bars->fixed_full, x0, kt * kT, b, pol);
+      int i = 0;
+      bool ok = true;
+      for (; i < n && ok; ++i) {
+        const int s = i % kKvStages;
+        const uint32_t ph = static_cast<uint32_t>(i / kKvStages) & 1u;
+        const uint32_t dph = static_cast<uint32_t>(i) & 1u;  // one dO slot
+        const int row = (i0 + i) * kT;
+        ok = mbar_wait(&bars->ring_empty[s], ph ^ 1u, abort_flag, p.st, kWhere | (1u << 16));
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars->ring_full[s], kTileBytes);
+        load_tile(smem + kFuSmQ + s * kTileBytes, &tm_q, &bars->ring_full[s], x0, row, b, pol);
+        ok = mbar_wait(&bars->do_empty[0], dph ^ 1u, abort_flag, p.st, kWhere | (11u << 16));
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars->do_full[0], kTileBytes);
+        load_tile(smem + kFuSmDo, &tm_do, &bars->do_full[0], x0, row, b, pol);
+      }
+      if (!ok) {
+        drain_wait(&bars->fixed_full, 0, p.st.limit);
+        for (int k2 = std::max(0, i - kKvStages); k2 <= i && k2 < n; ++k2)
+          drain_wait(&bars->ring_full[k2 % kKvStages], static_cast<uint32_t>(k2 / kKvStages) & 1u, p.st.limit);
+        for (int k2 = std::max(0, i - 1); k2 <= i && k2 < n; ++k2)
+          drain_wait(&bars->do_full[0], static_cast<uint32_t>(k2) & 1u, p.st.limit);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && n > 0) {
+      const uint32_t id_s = idesc_bf16(kT, kT, false, false);  // scores: both operands K-major
+      const uint32_t id_g = idesc_bf16(kT, kD, false, true);   // dK, dV: B MN-major
+      const uint32_t id_q = idesc_bf16(kT, kD, true, true);    // dQ: A (dS) and B (K) MN-major
+      const uint32_t sK = sbase + kFuSmK, sV = sbase + kFuSmV, sDs = sbase + kFuSmDs, sDo = sbase + kFuSmDo;
+      auto q_slot = [&](int i) { return sbase + kFuSmQ + (i % kKvStages) * kTileBytes; };
+      auto wait_q = [&](int i) {
+        const bool r = mbar_wait(&bars->ring_full[i % kKvStages], static_cast<uint32_t>(i / kKvStages) & 1u,
+                                 abort_flag, p.st, kWhere | (3u << 16));
+        tc_fence_after();
+        return r;
+      };
+      auto wait_do = [&](int i) {
+        const bool r = mbar_wait(&bars->do_full[0], static_cast<uint32_t>(i) & 1u, abort_flag, p.st,
+                                 kWhere | (12u << 16));
+        tc_fence_after();
+        return r;
+      };
+      bool ok = mbar_wait(&bars->fixed_full, 0, abort_flag, p.st, kWhere | (2u << 16));
+      if (ok) ok = wait_q(0);
+      if (ok) {
+        mma_ss_tile(tS, sK, q_slot(0), id_s, false);  // S^T(0) = K Q_0^T
+        tc_commit(&bars->s_full);
+      }
+      if (ok) ok = wait_do(0);
+      if (ok) {
+        mma_ss_tile(tDP, sV, sDo, id_s, false);  // dP^T(0) = V dO_0^T
+        tc_commit(&bars->dp_full);
+      }
+      for (int i = 0; i < n && ok; ++i) {
+        const uint32_t ph = static_cast<uint32_t>(i) & 1u;
+        ok = mbar_wait(&bars->pt_full, ph, abort_flag, p.st, kWhere | (4u << 16));
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T(i) dO_i; P^T K-step kk (queries 16kk..16kk+15) sits at columns 32(kk/2) + 8(kk%2)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t a = tS + 32 * (kk >> 1) + 8 * (kk & 1);
+          mma_ts(tDV, a, sdesc_sw128(sDo + kk * 2048, kColHalf, 1024), id_g, (i > 0 || kk > 0));
+        }
+        tc_commit(&bars->do_empty[0]);  // the dO slot may take dO(i+1)
+        if (i + 1 < n) {
+          ok = wait_q(i + 1);
+          if (!ok) break;
+          mma_ss_tile(tS, sK, q_slot(i + 1), id_s, false);  // S^T(i+1), after dV read P^T(i)
+          tc_commit(&bars->s_full);
+        }
+        // dS^T(i) is in shared memory; every compute thread loaded dP^T(i) before arriving
+        ok = mbar_wait(&bars->p_full, ph, abort_flag, p.st, kWhere | (13u << 16));
+        if (!ok) break;
+        tc_fence_after();
+        mma_ss_tile_mnmn(tDQ, sDs, sK, id_q);  // dQ(i) = dS(i) K
+        tc_commit(&bars->dq_full);
+        mma_ss_tile_mn(tDK, sDs, q_slot(i), id_g, i > 0);  // dK += dS^T(i) Q_i
+        tc_commit(&bars->ds_free);
+        tc_commit(&bars->ring_empty[i % kKvStages]);
+        if (i + 1 < n) {
+          ok = wait_do(i + 1);
+          if (ok) ok = mbar_wait(&bars->dq_free, ph, abort_flag, p.st, kWhere | (8u << 16));
+          if (!ok) break;
+          tc_fence_after();
+          mma_ss_tile(tDP, sV, sDo, id_s, false);  // dP^T(i+1), over the read dQ(i)
+          tc_commit(&bars->dp_full);
+        }
+      }
+      if (ok) tc_commit(&bars->acc_full);
+      tc_commit(&bars->mma_done);
+      drain_wait(&bars->mma_done, 0, p.st.limit);
+    }
+    __syncwarp();
+  } else if (warp == kFuReduceWarp) {
+    // Adds each staged 16 KB dQ block into the accumulator; frees its slot once read.
+    if (lane == 0 && n > 0) {
+      bool ok = true;
+      for (int i = 0; i < n && ok; ++i) {
+        const uint32_t ph = static_cast<uint32_t>(i) & 1u;
+        float* tile = p.dq_acc + b * p.dq_bs + h * p.dq_hs + static_cast<long long>(i0 + i) * (kT * kD);
+        for (int x = 0; x < 4 && ok; ++x) {  // blocks 0, 1, then 2, 3 reusing the slots
+          ok = mbar_wait(&bars->stg_full[x], ph, abort_flag, p.st, kWhere | (14u << 16));
+          if (!ok) break;
+          bulk_reduce_add_f32(tile + x * (kDqBlock / 4), sbase + kFuSmStg + (x & 1) * kDqBlock, kDqBlock);
+          bulk_commit();
+          bulk_wait_read<0>();
+          mbar_arrive(&bars->stg_free[x]);
+        }
+      }
+      bulk_wait_all();  // every reduction issued has completed
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- compute
+    const int x = warp >> 2;            // this warpgroup's query columns [32x, 32x + 32)
+    const int row = threadIdx.x & 127;  // key row of S^T/dP^T/dV/dK, query row of dQ: the TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint8_t* ds_tile = smem + kFuSmDs;
+    uint8_t* stg_row = smem + kFuSmStg + (x & 1) * kDqBlock + row * 128;
+    const int j = kt * kT + row;
+    const bool key_ok = j < p.Sk;  // rows past the keys: K is zero-filled there, P must be 0
+    const float c = p.scale_log2;
+    auto load_stats = [&](int i, float& l2v, float& dlv) {
+      const int q = (i0 + i) * kT + 32 * x + lane;
+      l2v = lse2_of(p, b, h, q);
+      dlv = (q < p.Sq) ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + q) : 0.f;
+    };
+    float nl2 = 0.f, ndl = 0.f;
+    if (n > 0) load_stats(0, nl2, ndl);
+    bool ok = true;
+    for (int i = 0; i < n && ok; ++i) {
+      const uint32_t ph = static_cast<uint32_t>(i) & 1u;
+      const int it = i0 + i;            // query tile
+      const int qx = it * kT + 32 * x;  // first query of this warpgroup's columns
+      const float l2v = nl2, dlv = ndl;
+      if (i + 1 < n) load_stats(i + 1, nl2, ndl);
+      ok = warp_all(mbar_wait(&bars->s_full, ph, abort_flag, p.st, kWhere | (5u << 16)));
+      if (!ok) break;
+      tc_fence_after();
+      const bool diag = p.causal && (it == kt);
+      // Phase 1: P^T, into this warpgroup's own S^T columns (already read by it).
+      float pv[32];
+      {
+        uint32_t s[32];
+        tmem_ld_x32(tS + lane_off + 32 * x, s);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float l2 = __shfl_sync(0xffffffffu, l2v, e);
+          float pe = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2));
+          if ((diag && qx + e < j) || !key_ok) pe = 0.f;
+          pv[e] = pe;
+        }
+      }
+      {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(pv[e], pv[e + 1]);
+        tmem_st_x16_nowait(tS + lane_off + 32 * x, pk);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->pt_full);  // dV(i) and S^T(i+1) may go
+      // Phase 2: dS^T = P^T (dP^T - Delta), into shared memory for dK and dQ.
+      ok = warp_all(mbar_wait(&bars->dp_full, ph, abort_flag, p.st, kWhere | (6u << 16)));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dk[16];
+      {
+        uint32_t dp[32];
+        tmem_ld_x32(tDP + lane_off + 32 * x, dp);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float d0 = __shfl_sync(0xffffffffu, dlv, e);
+          const float d1 = __shfl_sync(0xffffffffu, dlv, e + 1);
+          dk[e >> 1] =
+              pack_bf16x2(pv[e] * (__uint_as_float(dp[e]) - d0), pv[e + 1] * (__uint_as_float(dp[e + 1]) - d1));
+        }
+      }
+      if (i > 0) {
+        ok = warp_all(mbar_wait(&bars->ds_free, ph ^ 1u, abort_flag, p.st, kWhere | (9u << 16)));
+        if (!ok) break;
+      }
+      st_tile_quarter_row(ds_tile, row, x, dk);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);  // also: dP^T(i) is in registers, its columns may take dQ(i)
+      // Phase 3: row `row` of dQ(i) (TMEM lane = query row), columns [32x, 32x + 32), staged for the reducer.
+      ok = warp_all(mbar_wait(&bars->dq_full, ph, abort_flag, p.st, kWhere | (7u << 16)));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t g[32];
+      tmem_ld_x32(tDQ + lane_off + 32 * x, g);
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);
+      // slot x & 1 is free once the other warpgroup's block in it was read:
+      // warpgroups 0/1 wait for 2/3's block of tile i-1, 2/3 for 0/1's block of tile i.
+      if (x < 2) {
+        if (i > 0) ok = warp_all(mbar_wait(&bars->stg_free[x + 2], ph ^ 1u, abort_flag, p.st, kWhere | (15u << 16)));
+      } else {
+        ok = warp_all(mbar_wait(&bars->stg_free[x - 2], ph, abort_flag, p.st, kWhere | (15u << 16)));
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        *reinterpret_cast<float4*>(stg_row + ((ch ^ (row & 7)) << 4)) =
+            make_float4(__uint_as_float(g[4 * ch]) * p.scale, __uint_as_float(g[4 * ch + 1]) * p.scale,
+                        __uint_as_float(g[4 * ch + 2]) * p.scale, __uint_as_float(g[4 * ch + 3]) * p.scale);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->stg_full[x]);
+    }
+    // Epilogue: warpgroups 0/1 write dV columns [0,64)/[64,128), 2/3 write dK (scaled).
+    const bool valid = j < p.Sk;
+    const int half = x & 1;
+    const long long off = b * p.g_bs + static_cast<long long>(j) * p.g_rs + h * kD + 64 * half;
+    void* gdst = x < 2 ? p.g1 : p.g0;
+    const float mul = x < 2 ? 1.f : p.scale;
+    const uint32_t tacc = (x < 2 ? tDV : tDK) + lane_off + 64 * half;
+    if (n == 0) {
+      if (valid) store_zero(gdst, off, 64, p.grad_mode);
+    } else if (ok) {
+      ok = warp_all(mbar_wait(&bars->acc_full, 0, abort_flag, p.st, kWhere | (10u << 16)));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t a[32];
+          tmem_ld_x32(tacc + ch * 32, a);
+          if (valid) store_grad_chunk(gdst, off + ch * 32, a, mul, p.grad_mode);
+        }
+      }
+    }
+  }
+  teardown(tbase, warp);
+}
+
+// Tiled fp32 dQ accumulator (the fused pass's layout) -> bf16 [B, S, H, D].
+// One thread per 4 consecutive values of a row.
+__global__ void __launch_bounds__(256) dq_untile_kernel(const float* __restrict__ acc, long long tile_hs,
+                                                        long long tile_bs, __nv_bfloat16* __restrict__ dq,
+                                                        long long rs, long long bs, int B, int H, int S) {
+  const long long n = static_cast<long long>(B) * S * H * (kD / 4);
+  for (long long w = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; w < n;
+       w += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c4 = static_cast<int>(w % (kD / 4));  // four-float chunk of the row, 0..31
+    const long long rest = w / (kD / 4);
+    const int h = static_cast<int>(rest % H);
+    const long long bs_ = rest / H;
+    const int s = static_cast<int>(bs_ % S);
+    const int b = static_cast<int>(bs_ / S);
+    const int r = s & (kT - 1), x = c4 >> 3, ch = c4 & 7;
+    const float4 v = __ldg(reinterpret_cast<const float4*>(acc + b * tile_bs + h * tile_hs +
+                                                           static_cast<long long>(s / kT) * (kT * kD) + x * 4096 +
+                                                           r * 32 + ((ch ^ (r & 7)) << 2)));
+    uint2 u;
+    u.x = pack_bf16x2(v.x, v.y);
+    u.y = pack_bf16x2(v.z, v.w);
+    *reinterpret_cast<uint2*>(dq + b * bs + static_cast<long long>(s) * rs + h * kD + c4 * 4) = u;
+  }
+}
+
 // ============================================================== dQ pass
 // TMEM: Q [0,64) and dO [64,128) as A operands, S [128,256), dP [256,384),
 // dQ [384,512). Shared memory: a 3-slot ring of (K_j, V_j), dS.
@@ -684,6 +1053,9 @@ Params base_params(const BwdLaunch& a) {
   p.f1 = nullptr;
   p.f_rs = 0;
   p.f_bs = 0;
+  p.dq_acc = nullptr;
+  p.dq_hs = 0;
+  p.dq_bs = 0;
   p.B = a.B;
   p.H = a.H;
   p.Sq = a.Sq;
@@ -726,6 +1098,49 @@ int launch_attn_bwd_dkdv(const BwdLaunch& a, cudaStream_t stream) {
   const long long grid = static_cast<long long>((a.Sk + kT - 1) / kT) * a.B * a.H;
   if (grid > 0x7fffffffLL) return -1;
   attn_bwd_dkdv_kernel<<<static_cast<unsigned>(grid), kThreads, kKvSmem, stream>>>(tk, tv, tq, tdo, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+int launch_attn_bwd_fused(const BwdLaunch& a, cudaStream_t stream) {
+  if (a.Sk == 0) return 0;
+  CUtensorMap tk, tv, tq, tdo;
+  memset(&tq, 0, sizeof(tq));
+  memset(&tdo, 0, sizeof(tdo));
+  int rc;
+  if ((rc = make_tma_map_bf16(&tk, a.k, a.B, a.Sk, a.H * kD, kT)) != 0) return rc;
+  if ((rc = make_tma_map_bf16(&tv, a.v, a.B, a.Sk, a.H * kD, kT)) != 0) return rc;
+  if (a.Sq > 0) {
+    if ((rc = make_tma_map_bf16(&tq, a.q, a.B, a.Sq, a.H * kD, kT)) != 0) return rc;
+    if ((rc = make_tma_map_bf16(&tdo, a.dO, a.B, a.Sq, a.H * kD, kT)) != 0) return rc;
+  }
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_bwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFuSmem) !=
+        cudaSuccess)
+      return -4;
+    attr = true;
+  }
+  Params p = base_params(a);
+  p.g0 = a.dk;
+  p.g1 = a.dv;
+  p.g_rs = a.dkv_row_stride;
+  p.g_bs = a.dkv_batch_stride;
+  p.dq_acc = static_cast<float*>(a.dq);
+  p.dq_hs = a.dq_row_stride;    // tile head stride
+  p.dq_bs = a.dq_batch_stride;  // tile batch stride
+  const long long grid = static_cast<long long>((a.Sk + kT - 1) / kT) * a.B * a.H;
+  if (grid > 0x7fffffffLL) return -1;
+  attn_bwd_fused_kernel<<<static_cast<unsigned>(grid), kFuThreads, kFuSmem, stream>>>(tk, tv, tq, tdo, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+int launch_dq_untile(const float* acc, long long tile_hs, long long tile_bs, void* dq, long long rs, long long bs,
+                     int B, int H, int S, cudaStream_t stream) {
+  const long long n = static_cast<long long>(B) * S * H * (kD / 4);
+  if (n == 0) return 0;
+  const long long blocks = std::min<long long>((n + 255) / 256, 152LL * 16);
+  dq_untile_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      acc, tile_hs, tile_bs, static_cast<__nv_bfloat16*>(dq), rs, bs, B, H, S);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

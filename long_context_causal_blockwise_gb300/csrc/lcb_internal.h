@@ -50,6 +50,13 @@ struct BwdLaunch {
 };
 int launch_attn_bwd_dkdv(const BwdLaunch& a, cudaStream_t stream);
 int launch_attn_bwd_dq(const BwdLaunch& a, cudaStream_t stream);
+// One pass: dK/dV as grad_mode says; dQ is added into the tiled fp32
+// accumulator a.dq (a.dq_row_stride / a.dq_batch_stride carry its tile head /
+// batch strides in floats).
+int launch_attn_bwd_fused(const BwdLaunch& a, cudaStream_t stream);
+// Tiled fp32 dQ accumulator -> bf16 [B, S, H, D] rows (strides in elements).
+int launch_dq_untile(const float* acc, long long tile_hs, long long tile_bs, void* dq, long long rs, long long bs,
+                     int B, int H, int S, cudaStream_t stream);
 
 int launch_bwd_preprocess(const void* o, const void* dO, long long row_stride, long long batch_stride, float* delta,
                           long long d_head_stride, long long d_batch_stride, int B, int H, int S, cudaStream_t stream);

@@ -19,10 +19,11 @@ arithmetic runs in libattn.so kernels:
                           bf16 block result then attn_lse_merge)
            end          : lcb_cast_f32_bf16 of the accumulator
   backward Delta from the final bf16 O (attn_bwd_preprocess), then per task
-           attn_bwd_ex with the rank's FINAL merged LSE and Delta; fp32
-           gradients are stored at step 0 and accumulated after, dQ into the
-           querying rank's rows and dK/dV into the owning rank's rows; a cast
-           to bf16 ends it.
+           the one-pass backward (attn_bwd_fused_ex) with the rank's FINAL
+           merged LSE and Delta; dK/dV in fp32, stored at step 0 and
+           accumulated after into the owning rank's rows; dQ added into the
+           querying rank's tiles of one zeroed tiled accumulator; a cast
+           (lcb_dq_untile for dQ) to bf16 ends it.
 
 Outputs stay in zigzag order, the layout each rank would hold.
 """
@@ -91,14 +92,19 @@ def zigzag_attention_fwd(qz, kz, vz, plan, scale=None, o_acc=None, lse=None, o_b
     return o, lse, o_acc
 
 
-def zigzag_attention_bwd(qz, kz, vz, oz, lse, doz, plan, scale=None, delta=None, grads32=None, grads=None):
+def zigzag_attention_bwd(qz, kz, vz, oz, lse, doz, plan, scale=None, delta=None, grads32=None, grads=None,
+                         fused=True, dq_tiles=None):
     """Backward of the emulated ring; all tensors in zigzag order.
 
+    fused=True runs each task as the one-pass backward, every task adding its
+    dQ into one tiled fp32 accumulator (needs chunks of a multiple of 128
+    rows; otherwise, or with fused=False, the deterministic two-pass form).
     Returns (dq, dk, dv) bf16 [1, S, H, D].
     """
     B, S, H, D = qz.shape
     scale = D ** -0.5 if scale is None else scale
     dev = qz.device
+    fused = fused and plan.c % 128 == 0  # query blocks must start on accumulator tiles
     delta = torch.empty((1, H, S), dtype=torch.float32, device=dev) if delta is None else delta
     if grads32 is None:
         grads32 = tuple(torch.empty((1, S, H, D), dtype=torch.float32, device=dev) for _ in range(3))
@@ -106,12 +112,22 @@ def zigzag_attention_bwd(qz, kz, vz, oz, lse, doz, plan, scale=None, delta=None,
         grads = tuple(torch.empty_like(qz) for _ in range(3))
     dq32, dk32, dv32 = grads32
     _lib.attn_bwd_preprocess(oz, doz, delta)
+    if fused:
+        if dq_tiles is None:
+            dq_tiles = _lib.dq_tiles_zeros(1, H, S, dev)
+        else:
+            _lib.dq_tiles_zero_(dq_tiles)  # the fused pass only ever adds into dQ
     for t in plan.order:
         qs = slice(t["q_off"], t["q_off"] + t["q_len"])
         ks = slice(t["k_off"], t["k_off"] + t["k_len"])
+        dq_t = dq_tiles[:, :, t["q_off"] // 128:] if fused else dq32[:, qs]
         _lib.attn_bwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], lse[:, :, qs], delta[:, :, qs], doz[:, qs],
-                         dq32[:, qs], dk32[:, ks], dv32[:, ks], bool(t["causal"]), scale,
-                         accumulate=t["step"] > 0)
-    for g32, g in zip(grads32, grads):
+                         dq_t, dk32[:, ks], dv32[:, ks], bool(t["causal"]), scale,
+                         accumulate=t["step"] > 0, passes="fused" if fused else "both")
+    if fused:
+        _lib.dq_untile(dq_tiles, grads[0])
+    else:
+        _lib.cast_f32_bf16(dq32, grads[0])
+    for g32, g in zip(grads32[1:], grads[1:]):
         _lib.cast_f32_bf16(g32, g)
     return grads

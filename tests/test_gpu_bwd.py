@@ -7,7 +7,7 @@ import torch
 import oracle
 import long_context_causal_blockwise_gb300 as lcb
 from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo, sample_rows
-from parity import assert_bf16_close, assert_lse_close, head64, map_heads, rows_budget, to64
+from parity import assert_bf16_close, assert_lse_close, err_stats, head64, map_heads, rows_budget, to64
 
 pytestmark = pytest.mark.gpu
 D = 128
@@ -137,3 +137,106 @@ def test_config2_sampled_rows_backward():
     tol = 1e-2 * sdo.norm(dim=-1, keepdim=True)
     assert ((sdv - sdo).norm(dim=-1, keepdim=True) <= tol).all()
     assert (sdk.norm(dim=-1) <= 1e-2 * dk.float().norm(dim=(1, 3))).all()
+
+
+def _stats(q, k, v, do, causal, scale):
+    B, Sq, H, _ = q.shape
+    o = torch.empty(B, Sq, H, D, device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty(B, H, Sq, device="cuda")
+    lcb.attn_fwd_ex(q, k, v, o, lse, causal, scale)
+    delta = torch.empty(B, H, Sq, device="cuda")
+    lcb.attn_bwd_preprocess(o, do, delta)
+    return lse, delta
+
+
+def untile_f32(tiles, S):
+    """The fused pass's tiled dQ accumulator as fp32 [B, S, H, D], undoing the
+    documented layout (block x = columns [32x, 32x+32), row r, four-float
+    chunk c at position c ^ (r & 7))."""
+    B, H, T, _ = tiles.shape
+    t = tiles.view(B, H, T, 4, 128, 8, 4)
+    r = torch.arange(128, device=tiles.device)
+    c = torch.arange(8, device=tiles.device)
+    pos = c[None, :] ^ (r[:, None] & 7)  # [128, 8]: stored position of chunk c in row r
+    g = t[:, :, :, :, r[:, None], pos, :]  # [B, H, T, 4, 128, 8, 4]
+    out = g.permute(0, 2, 4, 1, 3, 5, 6).reshape(B, T * 128, H, D)
+    return out[:, :S]
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,causal", [(2, 3, 700, 700, True), (1, 2, 300, 520, False),
+                                              (1, 2, 130, 70, False), (1, 1, 1, 1, True)])
+def test_fused_pass_vs_two_pass_and_oracle(B, H, Sq, Sk, causal):
+    """The one-pass backward: dK/dV bit-identical to the two-pass dK/dV pass
+    (same products in the same order), dQ (bulk fp32 reductions into the tiled
+    accumulator) within fp32 rounding of the two-pass dQ, and all three
+    against the oracle; lcb_dq_untile gives the accumulator's bf16 rows."""
+    scale = D ** -0.5
+    g = torch.Generator(device="cuda").manual_seed(Sq * 7 + Sk)
+    mk = lambda n: torch.randn(B, n, H, D, generator=g, device="cuda").to(torch.bfloat16)  # noqa: E731
+    q, k, v, do = mk(Sq), mk(Sk), mk(Sk), mk(Sq)
+    lse, delta = _stats(q, k, v, do, causal, scale)
+    f32 = lambda n: torch.full((B, n, H, D), 7.0, device="cuda")  # noqa: E731
+    tiles, dk1, dv1 = lcb.dq_tiles_zeros(B, H, Sq, "cuda"), f32(Sk), f32(Sk)
+    lcb.attn_bwd_ex(q, k, v, lse, delta, do, tiles, dk1, dv1, causal, scale, accumulate=False, passes="fused")
+    dq2, dk2, dv2 = f32(Sq), f32(Sk), f32(Sk)
+    lcb.attn_bwd_ex(q, k, v, lse, delta, do, dq2, dk2, dv2, causal, scale, accumulate=False)
+    dq16 = lcb.dq_untile(tiles, torch.empty_like(q))
+    torch.cuda.synchronize()
+    dq1 = untile_f32(tiles, Sq)
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    assert torch.allclose(dq1, dq2, rtol=1e-4, atol=1e-5)
+    assert torch.equal(dq16, dq1.to(torch.bfloat16))
+    ref = oracle.attn_bwd(to64(q), to64(k), to64(v), to64(do), causal, scale)
+    assert_bf16_close(to64(dq1), ref["dq"], "dQ fused")
+    assert_bf16_close(to64(dk1), ref["dk"], "dK fused")
+    assert_bf16_close(to64(dv1), ref["dv"], "dV fused")
+
+
+def test_fused_pass_adds_into_dq_and_masks_ragged_keys():
+    """dQ is added into (two calls give twice one call), and a ragged key tile
+    whose zero-filled rows would score exp(-LSE) = inf for very negative LSE
+    leaves everything finite."""
+    B, H, Sq, Sk = 1, 2, 160, 70
+    scale = D ** -0.5
+    k = torch.ones(B, Sk, H, D, device="cuda", dtype=torch.bfloat16)
+    q = torch.full((B, Sq, H, D), -150.0 / (D * scale), device="cuda").to(torch.bfloat16)  # scores about -150
+    g = torch.Generator(device="cuda").manual_seed(11)
+    v = torch.randn(B, Sk, H, D, generator=g, device="cuda").to(torch.bfloat16)
+    do = torch.randn(B, Sq, H, D, generator=g, device="cuda").to(torch.bfloat16)
+    lse, delta = _stats(q, k, v, do, False, scale)
+    assert (lse < -140).all()
+    tiles = lcb.dq_tiles_zeros(B, H, Sq, "cuda")
+    dk = torch.empty(B, Sk, H, D, device="cuda", dtype=torch.bfloat16)
+    dv = torch.empty_like(dk)
+    lcb.attn_bwd_ex(q, k, v, lse, delta, do, tiles, dk, dv, False, scale, passes="fused")
+    once = untile_f32(tiles, Sq).clone()
+    lcb.attn_bwd_ex(q, k, v, lse, delta, do, tiles, dk, dv, False, scale, passes="fused")
+    torch.cuda.synchronize()
+    twice = untile_f32(tiles, Sq)
+    for t in (once, dk, dv):
+        assert torch.isfinite(t).all()
+    assert torch.allclose(twice, 2 * once, rtol=1e-6, atol=1e-6)
+    # the two-pass form masks the ragged keys explicitly: same dK/dV bits, dQ within fp32 rounding
+    dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(dk), torch.empty_like(dv)
+    lcb.attn_bwd_ex(q, k, v, lse, delta, do, dq2, dk2, dv2, False, scale)
+    torch.cuda.synchronize()
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    assert torch.allclose(once.to(torch.bfloat16).float(), dq2.float(), rtol=2e-2, atol=1e-3)
+    # against the oracle: |dK| is about 1 here, so relative L2 (bf16 rounding); dQ is 0 up to the rounding of dS
+    ref = oracle.attn_bwd(to64(q), to64(k), to64(v), to64(do), False, scale)
+    for got, want, name in ((dk, ref["dk"], "dK"), (dv, ref["dv"], "dV")):
+        _, _, rel = err_stats(to64(got), want)
+        assert rel <= 1e-2, f"{name} fused, ragged keys: rel-L2 {rel:.3e}"
+    assert np.abs(to64(once) - ref["dq"]).max() <= 2e-2
+
+
+def test_monolithic_backward_two_calls_agree():
+    """attn_bwd (fused, fp32 atomics for dQ) is repeatable to within bf16
+    rounding; dK and dV are bit-identical."""
+    q, k, v, do = gaussian_qkvdo(1, 4, 1024, D, seed=21)
+    o, lse = lcb.attn_fwd(q, k, v)
+    g1 = lcb.attn_bwd(q, k, v, o, lse, do)
+    g2 = lcb.attn_bwd(q, k, v, o, lse, do)
+    torch.cuda.synchronize()
+    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+    assert (g1[0].float() - g2[0].float()).abs().max().item() <= 2 ** -8 * g1[0].float().abs().max().item()
