@@ -78,6 +78,13 @@ typedef struct lcb_task {
   int32_t causal;
 } lcb_task;
 
+/* One block of attn_fwd_group: query rows [q_off, q_off + q_len) against key
+ * rows [k_off, k_off + k_len) of the shared tensors; o_dtype as attn_fwd_ex's. */
+typedef struct lcb_fwd_task {
+  int32_t q_off, q_len, k_off, k_len;
+  int32_t causal, o_dtype;
+} lcb_fwd_task;
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* attn_status_string(int status);
 
@@ -110,6 +117,24 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
                 long long kv_row_stride, long long kv_batch_stride, long long o_row_stride,
                 long long o_batch_stride, int o_dtype, long long lse_head_stride, long long lse_batch_stride,
                 void* stream);
+
+/*
+ * attn_fwd_group — several attn_fwd_ex blocks over the same tensors in ONE
+ * launch: the tasks of a ring step, [SP] / [ZZ], run side by side so that the
+ * grid fills whole waves of the GPU instead of one partial wave per block.
+ * q, k, v, o, lse as attn_fwd_ex's, holding q_rows query/output rows and
+ * k_rows key rows; strides likewise. tasks: HOST array of n_tasks <= 16.
+ * Each task is an attn_fwd_ex block on its row ranges (causal needs
+ * q_len == k_len, in task-local indices); query ranges of different tasks
+ * must not overlap (LCB_ERR_ARG); all tasks write bf16, or all write fp32
+ * (LCB_DTYPE_F32 or LCB_OUT_F32_MERGE, mixed freely). k_len == 0 behaves as
+ * in attn_fwd_ex. The library orders the tasks itself (longest CTAs first).
+ */
+int attn_fwd_group(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int q_rows,
+                   int k_rows, int D, float scale, long long q_row_stride, long long q_batch_stride,
+                   long long kv_row_stride, long long kv_batch_stride, long long o_row_stride,
+                   long long o_batch_stride, long long lse_head_stride, long long lse_batch_stride,
+                   const lcb_fwd_task* tasks, int n_tasks, void* stream);
 
 /* Bytes of device workspace attn_bwd needs: Delta (fp32 [B,H,S]) and the
  * fused pass's tiled fp32 dQ accumulator (B*H*ceil(S/128) tiles of 128x128);

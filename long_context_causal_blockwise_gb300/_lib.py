@@ -34,6 +34,10 @@ class LcbTask(ctypes.Structure):
                 ("rank", "step", "src", "kind", "q_off", "q_len", "k_off", "k_len", "causal")]
 
 
+class LcbFwdTask(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("q_off", "q_len", "k_off", "k_len", "causal", "o_dtype")]
+
+
 class AttnError(RuntimeError):
     def __init__(self, fn, status, msg):
         super().__init__(f"{fn} failed: {msg} ({status})")
@@ -65,6 +69,8 @@ _SIGNATURES = {
     "attn_bwd_dq_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _I,
                         _LL, _LL, _LL, _LL, _P], _I),
     "attn_lse_merge": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _LL, _LL, _LL, _LL, _LL, _LL, _LL, _LL, _P], _I),
+    "attn_fwd_group": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _LL, _LL,
+                        ctypes.POINTER(LcbFwdTask), _I, _P], _I),
     "zigzag_schedule": ([_I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(LcbTask)], _I),
     "lcb_permute_rows": ([_P, _P, _P, _I, _LL, _P], _I),
     "lcb_scatter_rows": ([_P, _P, _P, _I, _LL, _P], _I),
@@ -184,6 +190,35 @@ def attn_fwd_ex(q, k, v, o, lse, causal, scale, merge=False):
     _check("attn_fwd_ex", load().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk, D,
                                              int(causal), float(scale), qr, qb, kr, kb, orr, ob, o_dtype, lh, lb,
                                              _stream(q)))
+    return o, lse
+
+
+_OUT_MODES = {"bf16": LCB_DTYPE_BF16, "f32": LCB_DTYPE_F32, "merge": LCB_OUT_F32_MERGE}
+
+
+def attn_fwd_group(q, k, v, o, lse, tasks, scale):
+    """Several forward blocks over shared [B,S,H,D] views in one launch.
+
+    tasks: sequence of (q_off, q_len, k_off, k_len, causal, out) with out one
+    of "bf16", "f32", "merge" (o's dtype: bf16 for "bf16", fp32 otherwise);
+    query ranges must not overlap."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    qr, qb = _bshd(q, "q")
+    kr, kb = _bshd(k, "k")
+    if _bshd(v, "v") != (kr, kb):
+        raise ValueError("k and v must share strides")
+    orr, ob = _bshd(o, "o", o.dtype)
+    lh, lb = _bhs(lse, "lse")
+    arr = (LcbFwdTask * max(1, len(tasks)))()
+    for i, (qo, ql, ko, kl, causal, out) in enumerate(tasks):
+        want = torch.bfloat16 if out == "bf16" else torch.float32
+        if o.dtype != want:
+            raise ValueError(f"task output {out!r} needs o of dtype {want}")
+        arr[i] = LcbFwdTask(int(qo), int(ql), int(ko), int(kl), int(causal), _OUT_MODES[out])
+    _check("attn_fwd_group", load().attn_fwd_group(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Sq, Sk, D,
+                                                   float(scale), qr, qb, kr, kb, orr, ob, lh, lb, arr, len(tasks),
+                                                   _stream(q)))
     return o, lse
 
 

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -157,55 +158,130 @@ int lcb_take_device_status(unsigned int* where) {
   return rc != LCB_OK ? rc : static_cast<int>(bits);
 }
 
+// Checks the tensors shared by the tasks of a forward launch and fills `a`.
+static int prep_fwd(FwdLaunch* a, const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                    int q_rows, int k_rows, int D, float scale, long long q_row_stride, long long q_batch_stride,
+                    long long kv_row_stride, long long kv_batch_stride, long long o_row_stride,
+                    long long o_batch_stride, long long lse_head_stride, long long lse_batch_stride) {
+  if (B < 1 || H < 1 || q_rows < 0 || k_rows < 0) return LCB_ERR_ARG;
+  if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return LCB_ERR_ARG;
+  const long long HD = static_cast<long long>(H) * kHeadDim;
+  if (q_rows > 0) {
+    if (!o || !lse || !aligned16(o)) return LCB_ERR_ARG;
+    if (!stride_ok(o_row_stride) || !stride_ok(o_batch_stride) || HD > o_row_stride) return LCB_ERR_ARG;
+    if (lse_head_stride < 0 || lse_batch_stride < 0) return LCB_ERR_ARG;
+  }
+  if (q_rows > 0 && k_rows > 0) {
+    if (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v)) return LCB_ERR_ARG;
+    if (!stride_ok(q_row_stride) || !stride_ok(q_batch_stride) || !stride_ok(kv_row_stride) ||
+        !stride_ok(kv_batch_stride))
+      return LCB_ERR_ARG;
+    if (HD > q_row_stride || HD > kv_row_stride) return LCB_ERR_ARG;
+  }
+  a->q = {q, q_row_stride, q_batch_stride};
+  a->k = {k, kv_row_stride, kv_batch_stride};
+  a->v = {v, kv_row_stride, kv_batch_stride};
+  a->o = o;
+  a->lse = lse;
+  a->o_row_stride = o_row_stride;
+  a->o_batch_stride = o_batch_stride;
+  a->lse_head_stride = lse_head_stride;
+  a->lse_batch_stride = lse_batch_stride;
+  a->B = B;
+  a->H = H;
+  a->q_rows = q_rows;
+  a->k_rows = k_rows;
+  a->n_tasks = 0;
+  a->scale = scale;
+  return LCB_OK;
+}
+
+static int out_mode(int o_dtype) {
+  return o_dtype == LCB_OUT_F32_MERGE ? 2 : (o_dtype == LCB_DTYPE_F32 ? 1 : (o_dtype == LCB_DTYPE_BF16 ? 0 : -1));
+}
+
+// Enqueues the tasks of `a` (already checked): rows of tasks without keys are
+// filled with O = 0, LSE = -inf (or left alone in merge mode); the rest run as
+// one launch, heaviest per-CTA work first.
+static int run_fwd(FwdLaunch& a, const FwdTask* tasks, int n, cudaStream_t st) {
+  FwdTask order[kMaxFwdTasks];
+  int m = 0;
+  for (int i = 0; i < n; ++i) {
+    const FwdTask& t = tasks[i];
+    if (t.q_len == 0) continue;
+    if (t.k_len == 0) {
+      if (t.o_mode == 2) continue;  // an empty block leaves the accumulator unchanged
+      const size_t esz = t.o_mode == 1 ? 4 : 2;
+      void* o_rows = static_cast<char*>(a.o) + static_cast<long long>(t.q_off) * a.o_row_stride * esz;
+      const int rc = launch_fill_empty(o_rows, t.o_mode == 1, a.o_row_stride, a.o_batch_stride, a.lse + t.q_off,
+                                       a.lse_head_stride, a.lse_batch_stride, a.B, a.H, t.q_len, st);
+      if (rc != LCB_OK) return rc;
+      continue;
+    }
+    order[m++] = t;
+  }
+  if (m == 0) return LCB_OK;
+  const int rc = dev_status(&a.st);
+  if (rc != LCB_OK) return rc;
+  auto weight = [](const FwdTask& t) { return t.causal ? t.q_len : t.k_len; };  // key tiles of the longest CTA
+  std::stable_sort(order, order + m, [&](const FwdTask& x, const FwdTask& y) { return weight(x) > weight(y); });
+  for (int i = 0; i < m; ++i) a.tasks[i] = order[i];
+  a.n_tasks = m;
+  return launch_attn_fwd(a, st);
+}
+
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk,
                 int D, int causal, float scale, long long q_row_stride, long long q_batch_stride,
                 long long kv_row_stride, long long kv_batch_stride, long long o_row_stride,
                 long long o_batch_stride, int o_dtype, long long lse_head_stride, long long lse_batch_stride,
                 void* stream) {
-  if (B < 1 || H < 1 || Sq < 0 || Sk < 0) return LCB_ERR_ARG;
-  if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
   if (causal != 0 && causal != 1) return LCB_ERR_ARG;
   if (causal && Sq != Sk) return LCB_ERR_UNSUPPORTED;
-  if (o_dtype != LCB_DTYPE_BF16 && o_dtype != LCB_DTYPE_F32 && o_dtype != LCB_OUT_F32_MERGE) return LCB_ERR_UNSUPPORTED;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return LCB_ERR_ARG;
-  if (Sq == 0) return LCB_OK;
-  if (!o || !lse || !aligned16(o)) return LCB_ERR_ARG;
-  if (!stride_ok(o_row_stride) || !stride_ok(o_batch_stride)) return LCB_ERR_ARG;
-  if (lse_head_stride < 0 || lse_batch_stride < 0) return LCB_ERR_ARG;
-  if (static_cast<long long>(H) * kHeadDim > o_row_stride) return LCB_ERR_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (Sk == 0) {
-    if (o_dtype == LCB_OUT_F32_MERGE) return LCB_OK;  // an empty block leaves the accumulator unchanged
-    return finish(launch_fill_empty(o, o_dtype == LCB_DTYPE_F32, o_row_stride, o_batch_stride, lse, lse_head_stride,
-                                    lse_batch_stride, B, H, Sq, st),
-                  st);
-  }
-  if (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v)) return LCB_ERR_ARG;
-  if (!stride_ok(q_row_stride) || !stride_ok(q_batch_stride) || !stride_ok(kv_row_stride) ||
-      !stride_ok(kv_batch_stride))
-    return LCB_ERR_ARG;
-  if (static_cast<long long>(H) * kHeadDim > q_row_stride || static_cast<long long>(H) * kHeadDim > kv_row_stride)
-    return LCB_ERR_ARG;
+  const int mode = out_mode(o_dtype);
+  if (mode < 0) return LCB_ERR_UNSUPPORTED;
   FwdLaunch a;
-  a.q = {q, q_row_stride, q_batch_stride};
-  a.k = {k, kv_row_stride, kv_batch_stride};
-  a.v = {v, kv_row_stride, kv_batch_stride};
-  a.o = o;
-  a.lse = lse;
-  a.o_row_stride = o_row_stride;
-  a.o_batch_stride = o_batch_stride;
-  a.lse_head_stride = lse_head_stride;
-  a.lse_batch_stride = lse_batch_stride;
-  a.B = B;
-  a.H = H;
-  a.Sq = Sq;
-  a.Sk = Sk;
-  a.causal = causal;
-  a.o_mode = o_dtype == LCB_OUT_F32_MERGE ? 2 : (o_dtype == LCB_DTYPE_F32 ? 1 : 0);
-  a.scale = scale;
-  int rc = dev_status(&a.st);
+  int rc = prep_fwd(&a, q, k, v, o, lse, B, H, Sq, Sk, D, scale, q_row_stride, q_batch_stride, kv_row_stride,
+                    kv_batch_stride, o_row_stride, o_batch_stride, lse_head_stride, lse_batch_stride);
   if (rc != LCB_OK) return rc;
-  return finish(launch_attn_fwd(a, st), st);
+  if (Sq == 0) return LCB_OK;
+  const FwdTask t = {0, Sq, 0, Sk, causal, mode};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return finish(run_fwd(a, &t, 1, st), st);
+}
+
+int attn_fwd_group(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int q_rows,
+                   int k_rows, int D, float scale, long long q_row_stride, long long q_batch_stride,
+                   long long kv_row_stride, long long kv_batch_stride, long long o_row_stride,
+                   long long o_batch_stride, long long lse_head_stride, long long lse_batch_stride,
+                   const lcb_fwd_task* tasks, int n_tasks, void* stream) {
+  if (n_tasks < 0 || n_tasks > kMaxFwdTasks || (n_tasks > 0 && !tasks)) return LCB_ERR_ARG;
+  FwdLaunch a;
+  int rc = prep_fwd(&a, q, k, v, o, lse, B, H, q_rows, k_rows, D, scale, q_row_stride, q_batch_stride,
+                    kv_row_stride, kv_batch_stride, o_row_stride, o_batch_stride, lse_head_stride, lse_batch_stride);
+  if (rc != LCB_OK) return rc;
+  FwdTask t[kMaxFwdTasks];
+  int bf16_out = -1;  // all tasks write one output tensor: bf16, or fp32 (stored or merged)
+  for (int i = 0; i < n_tasks; ++i) {
+    const lcb_fwd_task& x = tasks[i];
+    const int mode = out_mode(x.o_dtype);
+    if (mode < 0) return LCB_ERR_UNSUPPORTED;
+    if (bf16_out >= 0 && bf16_out != (mode == 0)) return LCB_ERR_ARG;
+    bf16_out = mode == 0;
+    if (x.causal != 0 && x.causal != 1) return LCB_ERR_ARG;
+    if (x.causal && x.q_len != x.k_len) return LCB_ERR_UNSUPPORTED;
+    if (x.q_off < 0 || x.q_len < 0 || x.k_off < 0 || x.k_len < 0) return LCB_ERR_ARG;
+    if (static_cast<long long>(x.q_off) + x.q_len > q_rows || static_cast<long long>(x.k_off) + x.k_len > k_rows)
+      return LCB_ERR_ARG;
+    for (int j = 0; j < i; ++j) {  // query ranges must not overlap: each task owns its output rows
+      const lcb_fwd_task& y = tasks[j];
+      if (x.q_len > 0 && y.q_len > 0 && x.q_off < y.q_off + y.q_len && y.q_off < x.q_off + x.q_len)
+        return LCB_ERR_ARG;
+    }
+    t[i] = {x.q_off, x.q_len, x.k_off, x.k_len, x.causal, mode};
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return finish(run_fwd(a, t, n_tasks, st), st);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S, int D,

@@ -56,27 +56,35 @@ struct Bars {
 };
 constexpr uint32_t kSmemBytes = kSmBar + sizeof(Bars) + 1024;  // + alignment slack
 
+// One block of the launch: query rows [q_off, q_off + q_len) against key rows
+// [k_off, k_off + k_len) of the shared tensors; its CTAs start at cta0.
+struct Task {
+  int q_off, q_len, k_off, k_len, causal, o_mode;  // o_mode: 0 bf16 out, 1 fp32 out, 2 merge into fp32 (O, LSE)
+  int cta0;
+};
+
 struct Params {
   void* o;
   float* lse;
   long long o_rs, o_bs, l_hs, l_bs;
-  int B, H, Sq, Sk, causal, o_mode;  // o_mode: 0 bf16 out, 1 fp32 out, 2 merge into fp32 (O, LSE)
+  int B, H, n_tasks;
   float scale_log2;
   DevStatus st;
+  Task task[kMaxFwdTasks];
 };
 
 // Barrier ids for timeout reports (bits 16-23 of the where word), kernel id 1.
 constexpr uint32_t kWhere = 1u << 24;
 
-__device__ __forceinline__ void tile_counts(const Params& p, int q0, int& n0, int& n1) {
-  const int nk = (p.Sk + kBN - 1) / kBN;
+__device__ __forceinline__ void tile_counts(int Sq, int Sk, int causal, int q0, int& n0, int& n1) {
+  const int nk = (Sk + kBN - 1) / kBN;
   int n[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r0 = q0 + t * kBM;
-    if (r0 >= p.Sq) {
+    if (r0 >= Sq) {
       n[t] = 0;
-    } else if (p.causal) {
+    } else if (causal) {
       n[t] = min(nk, r0 / kBN + 1);
     } else {
       n[t] = nk;
@@ -102,17 +110,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
 
-  // Work item: query block qblk of (b, h). Head-major order (the K/V tiles every
-  // running CTA streams stay in L2); within a head the heaviest (latest) query
-  // blocks go first.
-  const int nq = (p.Sq + 2 * kBM - 1) / (2 * kBM);
-  const int bh = static_cast<int>(blockIdx.x / nq);
-  const int qblk = nq - 1 - static_cast<int>(blockIdx.x % nq);
+  // Work item: the task owning this CTA, then query block qblk of (b, h) in it.
+  // Tasks come heaviest first; within a task, head-major order (the K/V tiles
+  // every running CTA streams stay in L2), the heaviest (latest) query blocks
+  // of a head first. Row indices below are task-local; q_off / k_off place
+  // them in the shared tensors.
+  int ti = 0;
+  while (ti + 1 < p.n_tasks && static_cast<int>(blockIdx.x) >= p.task[ti + 1].cta0) ++ti;
+  const int Sq = p.task[ti].q_len, Sk = p.task[ti].k_len, causal = p.task[ti].causal;
+  const int q_off = p.task[ti].q_off, k_off = p.task[ti].k_off, o_mode = p.task[ti].o_mode;
+  const int local = static_cast<int>(blockIdx.x) - p.task[ti].cta0;
+  const int nq = (Sq + 2 * kBM - 1) / (2 * kBM);
+  const int bh = local / nq;
+  const int qblk = nq - 1 - local % nq;
   const int b = bh / p.H;
   const int h = bh % p.H;
   const int q0 = qblk * 2 * kBM;
   int n_t0, n_t1;
-  tile_counts(p, q0, n_t0, n_t1);
+  tile_counts(Sq, Sk, causal, q0, n_t0, n_t1);
   const int n_max = max(n_t0, n_t1);
 
   if (threadIdx.x == 0) {
@@ -155,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((t ? n_t1 : n_t0) == 0) continue;
         for (int half = 0; half < 2; ++half)
           tma_load_3d(smem + kSmQ + t * kTileBytes + half * kHalfBytes, &tm_q, &bars->q_full, x0 + half * 64,
-                      q0 + t * kBM, b);
+                      q_off + q0 + t * kBM, b);
       }
       int it = 0;
       bool ok = true;
@@ -171,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const CUtensorMap* map = kv == 0 ? &tm_k : &tm_v;
           for (int half = 0; half < 2; ++half)
             tma_load_3d_hint(smem + kSmKV + slot * kTileBytes + half * kHalfBytes, map, &bars->kv_full[slot],
-                             x0 + half * 64, j * kBN, b, pol);
+                             x0 + half * 64, k_off + j * kBN, b, pol);
         }
       }
       if (!ok) {
@@ -275,9 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t s[128];
       tmem_ld_x128(tS, s);
       const int kbase = j * kBN;
-      const bool need_mask = (p.causal && kbase + kBN - 1 > q0 + t * kBM) || (kbase + kBN > p.Sk);
+      const bool need_mask = (causal && kbase + kBN - 1 > q0 + t * kBM) || (kbase + kBN > Sk);
       if (need_mask) {
-        const int lim = p.causal ? min(qi + 1, p.Sk) : p.Sk;  // keys < lim are visible
+        const int lim = causal ? min(qi + 1, Sk) : Sk;  // keys < lim are visible (task-local)
 #pragma unroll
         for (int cc = 0; cc < 128; ++cc)
           if (kbase + cc >= lim) s[cc] = __float_as_uint(-INFINITY);
@@ -328,13 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && my_n > 0) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const bool valid = qi < p.Sq;
-      const long long lidx = b * p.l_bs + h * p.l_hs + qi;
+      const bool valid = qi < Sq;
+      const long long orow = static_cast<long long>(q_off + qi);  // row in the shared output tensors
+      const long long lidx = b * p.l_bs + h * p.l_hs + orow;
       const float lse_blk = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       // Merge mode (a fused ring step): O_acc <- (w_acc O_acc + w_blk O_blk) / (w_acc + w_blk)
       // with w_x = exp(LSE_x - max); here O_blk = O_tmem / l, so its weight absorbs 1/l.
       float c_acc = 0.f, c_blk = inv_l, lse_out = lse_blk;
-      if (p.o_mode == 2 && valid) {
+      if (o_mode == 2 && valid) {
         const float la = p.lse[lidx];
         const float mx = fmaxf(la, lse_blk);
         if (mx == -INFINITY) {
@@ -353,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t o[32];
         tmem_ld_x32(tO + ch * 32, o);
         if (valid) {
-          if (p.o_mode == 2) {
-            float* dst = static_cast<float*>(p.o) + b * p.o_bs + static_cast<long long>(qi) * p.o_rs + h * kD + ch * 32;
+          if (o_mode == 2) {
+            float* dst = static_cast<float*>(p.o) + b * p.o_bs + orow * p.o_rs + h * kD + ch * 32;
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               // an accumulator row with no keys yet (weight 0) is not read: its O may be unset
@@ -365,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      c_acc * a.w + c_blk * __uint_as_float(o[i + 3]));
               *reinterpret_cast<float4*>(dst + i) = v;
             }
-          } else if (p.o_mode == 1) {
-            float* dst = static_cast<float*>(p.o) + b * p.o_bs + static_cast<long long>(qi) * p.o_rs + h * kD + ch * 32;
+          } else if (o_mode == 1) {
+            float* dst = static_cast<float*>(p.o) + b * p.o_bs + orow * p.o_rs + h * kD + ch * 32;
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               float4 v = make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
@@ -374,8 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<float4*>(dst + i) = v;
             }
           } else {
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + b * p.o_bs + static_cast<long long>(qi) * p.o_rs +
-                                 h * kD + ch * 32;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + b * p.o_bs + orow * p.o_rs + h * kD + ch * 32;
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
               uint4 v;
@@ -422,11 +437,12 @@ __global__ void fill_empty_kernel(void* o, int o_f32, long long o_rs, long long 
 }  // namespace
 
 int launch_attn_fwd(const FwdLaunch& a, cudaStream_t stream) {
+  if (a.n_tasks < 1 || a.n_tasks > kMaxFwdTasks) return -1;
   CUtensorMap tq, tk, tv;
   int rc;
-  if ((rc = make_tma_map_bf16(&tq, a.q, a.B, a.Sq, a.H * kD, kBM)) != 0) return rc;
-  if ((rc = make_tma_map_bf16(&tk, a.k, a.B, a.Sk, a.H * kD, kBN)) != 0) return rc;
-  if ((rc = make_tma_map_bf16(&tv, a.v, a.B, a.Sk, a.H * kD, kBN)) != 0) return rc;
+  if ((rc = make_tma_map_bf16(&tq, a.q, a.B, a.q_rows, a.H * kD, kBM)) != 0) return rc;
+  if ((rc = make_tma_map_bf16(&tk, a.k, a.B, a.k_rows, a.H * kD, kBN)) != 0) return rc;
+  if ((rc = make_tma_map_bf16(&tv, a.v, a.B, a.k_rows, a.H * kD, kBN)) != 0) return rc;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
@@ -443,15 +459,17 @@ int launch_attn_fwd(const FwdLaunch& a, cudaStream_t stream) {
   p.l_bs = a.lse_batch_stride;
   p.B = a.B;
   p.H = a.H;
-  p.Sq = a.Sq;
-  p.Sk = a.Sk;
-  p.causal = a.causal;
-  p.o_mode = a.o_mode;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.st = a.st;
-  const long long nq = (a.Sq + 2 * kBM - 1) / (2 * kBM);
-  const long long grid = nq * a.B * a.H;
-  if (grid > 0x7fffffffLL) return -1;
+  long long grid = 0;
+  p.n_tasks = a.n_tasks;
+  for (int i = 0; i < a.n_tasks; ++i) {
+    const FwdTask& t = a.tasks[i];
+    p.task[i] = {t.q_off, t.q_len, t.k_off, t.k_len, t.causal, t.o_mode, static_cast<int>(grid)};
+    grid += static_cast<long long>((t.q_len + 2 * kBM - 1) / (2 * kBM)) * a.B * a.H;
+    if (grid > 0x7fffffffLL) return -1;
+  }
+  if (grid == 0) return 0;
   attn_fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }

@@ -22,13 +22,23 @@ struct RowView {
 // Returns 0 on success, a negative LCB status on failure.
 int make_tma_map_bf16(CUtensorMap* map, const RowView& v, int B, int rows, int HD, int box_rows);
 
+// One block of a forward launch (rows relative to the shared tensors).
+struct FwdTask {
+  int q_off, q_len, k_off, k_len, causal, o_mode;  // o_mode: 0 bf16, 1 fp32, 2 merge into fp32 (O, LSE)
+};
+constexpr int kMaxFwdTasks = 16;
+
+// q/o/lse views hold q_rows rows, k/v views k_rows; every task has k_len > 0,
+// tasks are ordered heaviest first and their query ranges do not overlap.
 struct FwdLaunch {
   RowView q, k, v;
   void* o;
   float* lse;
   long long o_row_stride, o_batch_stride;
   long long lse_head_stride, lse_batch_stride;
-  int B, H, Sq, Sk, causal, o_mode;  // 0 bf16, 1 fp32, 2 merge into fp32 (O, LSE)
+  int B, H, q_rows, k_rows;
+  int n_tasks;
+  FwdTask tasks[kMaxFwdTasks];
   float scale;
   DevStatus st;
 };

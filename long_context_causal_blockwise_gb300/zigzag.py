@@ -13,10 +13,12 @@ and no collective runs. Steps are executed step-major (all ranks' step 0, then
 step 1, ...), as the real ring would run them in parallel. Every piece of
 arithmetic runs in libattn.so kernels:
 
-  forward  step 0 (DIAG): attn_fwd_ex, causal, writing the fp32 accumulator
-           step s > 0   : attn_fwd_ex in merge mode, folding the block into the
-                          fp32 accumulator in its epilogue (or, unfused, a
-                          bf16 block result then attn_lse_merge)
+  forward  one attn_fwd_group launch per ring step s, its P tasks side by side:
+           s = 0 (DIAG): causal, writing the fp32 accumulator;
+           s > 0       : merge mode, folding each block into the fp32
+                         accumulator in the kernel epilogue
+           (unfused: attn_fwd_ex per task, a bf16 block result, then
+           attn_lse_merge)
            end          : lcb_cast_f32_bf16 of the accumulator
   backward Delta from the final bf16 O (attn_bwd_preprocess), then per task
            the one-pass backward (attn_bwd_fused_ex) with the rank's FINAL
@@ -62,8 +64,10 @@ def zigzag_attention_fwd(qz, kz, vz, plan, scale=None, o_acc=None, lse=None, o_b
     """Forward of the emulated ring on zigzag-ordered [1, S, H, D] bf16 inputs.
 
     Returns (o bf16, lse fp32 [1, H, S], o_acc fp32), all in zigzag order.
-    fused=True merges each step inside the forward kernel's epilogue; False
-    writes the block result and runs the separate merge kernel.
+    fused=True runs each ring step as ONE grouped launch of its P tasks
+    (attn_fwd_group) that merges into the accumulator in the kernel epilogue;
+    False runs one launch per task, writing the block result, then the
+    separate merge kernel.
     Buffers may be passed in to keep allocation out of a timed loop.
     """
     B, S, H, D = qz.shape
@@ -77,17 +81,22 @@ def zigzag_attention_fwd(qz, kz, vz, plan, scale=None, o_acc=None, lse=None, o_b
     o_blk = torch.empty((1, c2, H, D), dtype=torch.bfloat16, device=dev) if o_blk is None else o_blk
     lse_blk = torch.empty((1, H, c2), dtype=torch.float32, device=dev) if lse_blk is None else lse_blk
     o = torch.empty_like(qz) if o is None else o
-    for t in plan.order:
-        qs = slice(t["q_off"], t["q_off"] + t["q_len"])
-        ks = slice(t["k_off"], t["k_off"] + t["k_len"])
-        if t["step"] == 0:
-            _lib.attn_fwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], o_acc[:, qs], lse[:, :, qs], True, scale)
-        elif fused:
-            _lib.attn_fwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], o_acc[:, qs], lse[:, :, qs], False, scale, merge=True)
-        else:
-            n = t["q_len"]
-            _lib.attn_fwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], o_blk[:, :n], lse_blk[:, :, :n], False, scale)
-            _lib.attn_lse_merge(o_acc[:, qs], lse[:, :, qs], o_blk[:, :n], lse_blk[:, :, :n])
+    if fused:
+        # one launch per ring step: the P ranks' tasks of a step own disjoint query rows
+        for step in range(plan.P):
+            tasks = [(t["q_off"], t["q_len"], t["k_off"], t["k_len"], t["causal"], "f32" if step == 0 else "merge")
+                     for t in plan.order if t["step"] == step]
+            _lib.attn_fwd_group(qz, kz, vz, o_acc, lse, tasks, scale)
+    else:
+        for t in plan.order:
+            qs = slice(t["q_off"], t["q_off"] + t["q_len"])
+            ks = slice(t["k_off"], t["k_off"] + t["k_len"])
+            if t["step"] == 0:
+                _lib.attn_fwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], o_acc[:, qs], lse[:, :, qs], True, scale)
+            else:
+                n = t["q_len"]
+                _lib.attn_fwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], o_blk[:, :n], lse_blk[:, :, :n], False, scale)
+                _lib.attn_lse_merge(o_acc[:, qs], lse[:, :, qs], o_blk[:, :n], lse_blk[:, :, :n])
     _lib.cast_f32_bf16(o_acc, o)
     return o, lse, o_acc
 

@@ -81,6 +81,26 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.lcb_cast_f32_bf16(nul, nul, -1, nul) == _lib.LCB_ERR_ARG
 
 
+def test_fwd_group_argument_errors_need_no_gpu(lib):
+    """attn_fwd_group rejects bad task tables before any CUDA call."""
+    nul = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: every call below fails validation first
+
+    def call(tasks, q_rows=1024, k_rows=1024, n=None):
+        arr = (_lib.LcbFwdTask * max(1, len(tasks)))(*[_lib.LcbFwdTask(*t) for t in tasks])
+        return lib.attn_fwd_group(fake, fake, fake, fake, fake, 1, 2, q_rows, k_rows, 128, 0.1, 256, 0, 256, 0, 256,
+                                  0, 1024, 2048, arr, len(tasks) if n is None else n, nul)
+    F32, BF16, MERGE = _lib.LCB_DTYPE_F32, _lib.LCB_DTYPE_BF16, _lib.LCB_OUT_F32_MERGE
+    assert call([(0, 512, 0, 512, 0, F32), (256, 512, 0, 512, 0, F32)]) == _lib.LCB_ERR_ARG  # query rows overlap
+    assert call([(0, 512, 600, 512, 0, F32)]) == _lib.LCB_ERR_ARG                            # keys past k_rows
+    assert call([(-1, 16, 0, 16, 0, F32)]) == _lib.LCB_ERR_ARG                               # negative offset
+    assert call([(0, 256, 0, 256, 0, F32), (256, 256, 0, 256, 0, BF16)]) == _lib.LCB_ERR_ARG  # one output dtype
+    assert call([(0, 256, 0, 512, 1, MERGE)]) == _lib.LCB_ERR_UNSUPPORTED                    # causal needs a square
+    assert call([(0, 256, 0, 256, 0, 9)]) == _lib.LCB_ERR_UNSUPPORTED                        # unknown output
+    assert call([(0, 16, 0, 16, 0, F32)], n=17) == _lib.LCB_ERR_ARG                          # at most 16 tasks
+    assert call([]) == _lib.LCB_OK                                                           # nothing to do
+
+
 @pytest.mark.parametrize("S,P", [(8, 2), (16, 1), (48, 3), (256, 4), (256, 8), (131072, 8), (524288, 8)])
 def test_zigzag_schedule_matches_oracle_bit_exact(lib, S, P):
     perm, tasks = _lib.zigzag_schedule(S, P)

@@ -193,3 +193,38 @@ def test_config2_sampled_rows_forward():
     ref = oracle.attn_rows(to64(q), to64(k), to64(v), None, rows, True, D ** -0.5)
     assert_bf16_close(to64(o[:, rows]), ref["o"], "O C2 sampled")
     assert_lse_close(to64(lse[:, :, rows]), ref["lse"])
+
+
+def test_grouped_launch_equals_separate_calls():
+    """attn_fwd_group runs several blocks in one launch: every output equals
+    the attn_fwd_ex call of the same block bit for bit, for causal and
+    rectangular blocks, ragged lengths, fp32 store and merge outputs, and
+    blocks without keys (store: O = 0, LSE = -inf; merge: untouched)."""
+    B, H, S = 2, 3, 1500
+    g = torch.Generator(device="cuda").manual_seed(31)
+    q, k, v = (torch.randn(B, S, H, D, generator=g, device="cuda").to(torch.bfloat16) for _ in range(3))
+    scale = D ** -0.5
+    tasks = [(0, 300, 0, 300, 1, "f32"),       # causal diagonal block
+             (300, 256, 700, 513, 0, "f32"),   # rectangular, ragged keys
+             (556, 129, 0, 1500, 0, "merge"),  # merge into an accumulator, ragged queries
+             (685, 400, 100, 200, 0, "merge"),
+             (1085, 77, 0, 0, 0, "f32"),       # no keys: stored as empty
+             (1162, 60, 0, 0, 0, "merge"),     # no keys: accumulator untouched
+             (1222, 278, 1222, 278, 1, "f32")]
+    acc0 = torch.randn(B, S, H, D, generator=g, device="cuda")
+    lse0 = torch.randn(B, H, S, generator=g, device="cuda")
+    o1, l1 = acc0.clone(), lse0.clone()
+    lcb.attn_fwd_group(q, k, v, o1, l1, tasks, scale)
+    o2, l2 = acc0.clone(), lse0.clone()
+    for qo, ql, ko, kl, causal, out in tasks:
+        qs, ks = slice(qo, qo + ql), slice(ko, ko + kl)
+        lcb.attn_fwd_ex(q[:, qs], k[:, ks], v[:, ks], o2[:, qs], l2[:, :, qs], bool(causal), scale,
+                        merge=(out == "merge"))
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # and a store-mode block against the oracle
+    ref_o, ref_l = oracle.attn_fwd(to64(q[:, 300:556]), to64(k[:, 700:1213]), to64(v[:, 700:1213]), False, scale)
+    assert_bf16_close(to64(o1[:, 300:556]), ref_o, "O grouped block")
+    assert_lse_close(to64(l1[:, :, 300:556]), ref_l)
+    assert (o1[:, 1085:1162] == 0).all() and torch.isneginf(l1[:, :, 1085:1162]).all()
+    assert torch.equal(o1[:, 1162:1222], acc0[:, 1162:1222])
