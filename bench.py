@@ -460,7 +460,7 @@ def run_zigzag(args):
         "fwd_ms": {"ring_fused_merge": t_fwd_fused, "ring_merge_kernel": t_fwd_unfused, "monolithic": t_fwd_mono},
         "merge_ms_per_call": t_merge, "merge_rows": c2, "merge_gbs": merge_bytes / t_merge / 1e6,
         "merge_frac_of_hbm": merge_bytes / t_merge / 1e6 / hbm, "hbm_peak_source": src,
-        "launches_per_ring_step": "fwd: 1 (merge fused in the epilogue); bwd: 1 per task (one pass) + preprocess + untile"}),
+        "launches_per_ring_step": "fwd: 1 grouped launch of the P tasks (merge fused in the epilogue); bwd: 1 grouped one-pass launch of the P tasks; + preprocess, zeroing and untile once per pass"}),
           flush=True)
     return 0
 

@@ -85,6 +85,13 @@ typedef struct lcb_fwd_task {
   int32_t causal, o_dtype;
 } lcb_fwd_task;
 
+/* One block of attn_bwd_fused_group: query rows [q_off, q_off + q_len)
+ * (q_off a multiple of 128) against key rows [k_off, k_off + k_len). */
+typedef struct lcb_bwd_task {
+  int32_t q_off, q_len, k_off, k_len;
+  int32_t causal;
+} lcb_bwd_task;
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* attn_status_string(int status);
 
@@ -213,6 +220,25 @@ int attn_bwd_fused_ex(const void* q, const void* k, const void* v, const float* 
                       long long lse_batch_stride, int grad_mode, long long dq_tile_head_stride,
                       long long dq_tile_batch_stride, long long dkv_row_stride, long long dkv_batch_stride,
                       void* stream);
+
+/*
+ * attn_bwd_fused_group — several attn_bwd_fused_ex blocks over the same
+ * tensors in ONE launch (the tasks of a ring step, [SP] / [ZZ]). q, dO, lse,
+ * delta and the dQ accumulator cover q_rows query rows, k, v, dk, dv k_rows
+ * key rows; strides and grad_mode as attn_bwd_fused_ex's. tasks: HOST array
+ * of n_tasks <= 16; q_off must be a multiple of 128 (a task adds into the
+ * accumulator's tiles from q_off / 128 on); key ranges of different tasks
+ * must not overlap (each owns its dK/dV rows; LCB_ERR_ARG), query ranges may.
+ * A task without queries zeroes its dK/dV rows in the overwrite modes.
+ * The library orders the tasks itself (longest rows first).
+ */
+int attn_bwd_fused_group(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                         const void* dO, float* dq_tiles, void* dk, void* dv, int B, int H, int q_rows, int k_rows,
+                         int D, float scale, long long q_row_stride, long long q_batch_stride,
+                         long long kv_row_stride, long long kv_batch_stride, long long lse_head_stride,
+                         long long lse_batch_stride, int grad_mode, long long dq_tile_head_stride,
+                         long long dq_tile_batch_stride, long long dkv_row_stride, long long dkv_batch_stride,
+                         const lcb_bwd_task* tasks, int n_tasks, void* stream);
 
 /* lcb_dq_tiles_zero — zeroes n_floats of a tiled dQ accumulator (an async
  * memset on `stream`; dq_tiles 16-byte aligned). */

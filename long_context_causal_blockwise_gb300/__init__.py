@@ -3,7 +3,7 @@ training with sequence parallelism, as a C-ABI CUDA library (libattn.so) with a
 thin Python binding.
 
 Public calls (all run in this library's CUDA kernels):
-  attn_fwd, attn_fwd_ex, attn_fwd_group, attn_bwd, attn_bwd_ex, attn_bwd_preprocess, attn_bwd_noalloc,
+  attn_fwd, attn_fwd_ex, attn_fwd_group, attn_bwd, attn_bwd_ex, attn_bwd_group, attn_bwd_preprocess, attn_bwd_noalloc,
   dq_tiles_zeros / dq_tiles_zero_ / dq_untile (the one-pass backward's tiled dQ accumulator),
   attn_lse_merge, zigzag_schedule, permute_rows, cast_f32_bf16,
   zigzag_attention_fwd / zigzag_attention_bwd (the one-device zigzag ring).
@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     AttnError,
     attn_bwd,
     attn_bwd_ex,
+    attn_bwd_group,
     attn_bwd_noalloc,
     attn_bwd_noalloc_max_rows,
     attn_bwd_preprocess,

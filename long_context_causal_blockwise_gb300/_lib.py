@@ -38,6 +38,10 @@ class LcbFwdTask(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("q_off", "q_len", "k_off", "k_len", "causal", "o_dtype")]
 
 
+class LcbBwdTask(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("q_off", "q_len", "k_off", "k_len", "causal")]
+
+
 class AttnError(RuntimeError):
     def __init__(self, fn, status, msg):
         super().__init__(f"{fn} failed: {msg} ({status})")
@@ -62,6 +66,8 @@ _SIGNATURES = {
                      _LL, _LL, _LL, _LL, _P], _I),
     "attn_bwd_fused_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL,
                            _LL, _I, _LL, _LL, _LL, _LL, _P], _I),
+    "attn_bwd_fused_group": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL,
+                              _LL, _I, _LL, _LL, _LL, _LL, ctypes.POINTER(LcbBwdTask), _I, _P], _I),
     "lcb_dq_tiles_zero": ([_P, _LL, _P], _I),
     "lcb_dq_untile": ([_P, _LL, _LL, _P, _LL, _LL, _I, _I, _I, _P], _I),
     "attn_bwd_dkdv_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL,
@@ -330,6 +336,44 @@ def attn_bwd_ex(q, k, v, lse, delta, do, dq, dk, dv, causal, scale, accumulate=T
                                              _ptr(dk), _ptr(dv), B, H, Sq, Sk, D, int(causal), float(scale), qr, qb,
                                              kr, kb, lh, lb, grad_mode, dqr, dqb, dkr, dkb, _stream(q)))
     return dq, dk, dv
+
+
+def attn_bwd_group(q, k, v, lse, delta, do, dq_tiles, dk, dv, tasks, scale, accumulate=True):
+    """Several one-pass backward blocks over shared [B,S,H,D] views in one launch.
+
+    tasks: sequence of (q_off, q_len, k_off, k_len, causal), q_off a multiple
+    of 128, key ranges disjoint. dq_tiles: the tiled accumulator of all of q's
+    rows (dq_tiles_zeros), added into; dk/dv as in attn_bwd_ex(passes="fused")."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    qr, qb = _bshd(q, "q")
+    if _bshd(do, "do") != (qr, qb):
+        raise ValueError("q and do must share strides")
+    kr, kb = _bshd(k, "k")
+    if _bshd(v, "v") != (kr, kb):
+        raise ValueError("k and v must share strides")
+    lh, lb = _bhs(lse, "lse")
+    if _bhs(delta, "delta") != (lh, lb):
+        raise ValueError("lse and delta must share strides")
+    if dq_tiles.dtype != torch.float32 or dq_tiles.dim() != 4 or dq_tiles.shape[:2] != (B, H) \
+            or dq_tiles.shape[2] * 128 < Sq or dq_tiles.stride(3) != 1 or dq_tiles.stride(2) != 128 * 128:
+        raise ValueError("dq_tiles must be a tiled fp32 accumulator covering q (dq_tiles_zeros)")
+    gdt = dk.dtype
+    if dv.dtype != gdt:
+        raise ValueError("dk and dv must share a dtype")
+    if gdt == torch.float32:
+        grad_mode = LCB_GRAD_F32_ACCUM if accumulate else LCB_GRAD_F32_STORE
+    else:
+        grad_mode = LCB_GRAD_BF16
+    dkr, dkb = _bshd(dk, "dk", gdt)
+    if _bshd(dv, "dv", gdt) != (dkr, dkb):
+        raise ValueError("dk and dv must share strides")
+    arr = (LcbBwdTask * max(1, len(tasks)))(*[LcbBwdTask(*(int(x) for x in t)) for t in tasks])
+    _check("attn_bwd_fused_group", load().attn_bwd_fused_group(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(do), _ptr(dq_tiles), _ptr(dk), _ptr(dv), B, H, Sq,
+        Sk, D, float(scale), qr, qb, kr, kb, lh, lb, grad_mode, dq_tiles.stride(1), dq_tiles.stride(0), dkr, dkb, arr,
+        len(tasks), _stream(q)))
+    return dq_tiles, dk, dv
 
 
 def dq_tiles_zeros(B, H, S, device):

@@ -413,11 +413,27 @@ int attn_bwd_fused_ex(const void* q, const void* k, const void* v, const float* 
                       long long lse_batch_stride, int grad_mode, long long dq_tile_head_stride,
                       long long dq_tile_batch_stride, long long dkv_row_stride, long long dkv_batch_stride,
                       void* stream) {
+  const lcb_bwd_task t = {0, Sq, 0, Sk, causal};
+  return attn_bwd_fused_group(q, k, v, lse, delta, dO, dq_tiles, dk, dv, B, H, Sq, Sk, D, scale, q_row_stride,
+                              q_batch_stride, kv_row_stride, kv_batch_stride, lse_head_stride, lse_batch_stride,
+                              grad_mode, dq_tile_head_stride, dq_tile_batch_stride, dkv_row_stride,
+                              dkv_batch_stride, &t, 1, stream);
+}
+
+int attn_bwd_fused_group(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+                         const void* dO, float* dq_tiles, void* dk, void* dv, int B, int H, int q_rows, int k_rows,
+                         int D, float scale, long long q_row_stride, long long q_batch_stride,
+                         long long kv_row_stride, long long kv_batch_stride, long long lse_head_stride,
+                         long long lse_batch_stride, int grad_mode, long long dq_tile_head_stride,
+                         long long dq_tile_batch_stride, long long dkv_row_stride, long long dkv_batch_stride,
+                         const lcb_bwd_task* tasks, int n_tasks, void* stream) {
+  if (n_tasks < 0 || n_tasks > kMaxBwdTasks || (n_tasks > 0 && !tasks)) return LCB_ERR_ARG;
   // The accumulator is checked here; prep_bwd sees row strides that always pass.
   if (dq_tile_head_stride < 0 || dq_tile_batch_stride < 0 || (dq_tile_head_stride % 4) ||
       (dq_tile_batch_stride % 4))
     return LCB_ERR_ARG;
   void* dq = dq_tiles;
+  const int Sq = q_rows, Sk = k_rows, causal = 0;  // shared tensors; causality is per task
   const long long HD = static_cast<long long>(H) * kHeadDim;
   const long long dq_row_stride = HD, dq_batch_stride = HD * Sq;
   BwdLaunch a;
@@ -425,8 +441,44 @@ int attn_bwd_fused_ex(const void* q, const void* k, const void* v, const float* 
   if (rc != LCB_OK) return rc;
   a.dq_row_stride = dq_tile_head_stride;
   a.dq_batch_stride = dq_tile_batch_stride;
+  BwdTask order[kMaxBwdTasks];
+  int m = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return finish(launch_attn_bwd_fused(a, st), st);
+  for (int i = 0; i < n_tasks; ++i) {
+    const lcb_bwd_task& x = tasks[i];
+    if (x.causal != 0 && x.causal != 1) return LCB_ERR_ARG;
+    if (x.causal && x.q_len != x.k_len) return LCB_ERR_UNSUPPORTED;
+    if (x.q_off < 0 || x.q_len < 0 || x.k_off < 0 || x.k_len < 0 || (x.q_off % 128)) return LCB_ERR_ARG;
+    if (static_cast<long long>(x.q_off) + x.q_len > q_rows || static_cast<long long>(x.k_off) + x.k_len > k_rows)
+      return LCB_ERR_ARG;
+    for (int j = 0; j < i; ++j) {  // key ranges must not overlap: each task owns its dK/dV rows
+      const lcb_bwd_task& y = tasks[j];
+      if (x.k_len > 0 && y.k_len > 0 && x.k_off < y.k_off + y.k_len && y.k_off < x.k_off + x.k_len)
+        return LCB_ERR_ARG;
+    }
+  }
+  for (int i = 0; i < n_tasks; ++i) {
+    const lcb_bwd_task& x = tasks[i];
+    if (x.k_len == 0) continue;
+    if (x.q_len == 0) {  // no queries: dK = dV = 0 (overwrite modes), nothing added to dQ
+      if (grad_mode == LCB_GRAD_F32_ACCUM) continue;
+      const size_t esz = grad_mode == LCB_GRAD_BF16 ? 2 : 4;
+      for (int g = 0; g < 2; ++g) {
+        char* base = static_cast<char*>(g ? dv : dk) + static_cast<long long>(x.k_off) * dkv_row_stride * esz;
+        for (int b = 0; b < B; ++b) {
+          if (cudaMemset2DAsync(base + b * dkv_batch_stride * esz, dkv_row_stride * esz, 0, HD * esz, x.k_len, st) !=
+              cudaSuccess)
+            return LCB_ERR_CUDA;
+        }
+      }
+      continue;
+    }
+    order[m++] = {x.q_off, x.q_len, x.k_off, x.k_len, x.causal};
+  }
+  if (m == 0) return finish(LCB_OK, st);
+  auto weight = [](const BwdTask& t) { return t.q_len; };  // query tiles of the longest CTA
+  std::stable_sort(order, order + m, [&](const BwdTask& x, const BwdTask& y) { return weight(x) > weight(y); });
+  return finish(launch_attn_bwd_fused(a, order, m, q_rows, k_rows, st), st);
 }
 
 int lcb_dq_tiles_zero(float* dq_tiles, long long n_floats, void* stream) {

@@ -67,6 +67,12 @@ struct Bars {
   int abort;
 };
 
+// Fused pass: one block of the launch, query rows [q_off, q_off + q_len)
+// against key rows [k_off, k_off + k_len); its CTAs start at cta0.
+struct BwdTaskP {
+  int q_off, q_len, k_off, k_len, causal, cta0;
+};
+
 struct Params {
   const float* lse;
   const float* delta;
@@ -79,6 +85,8 @@ struct Params {
   long long g_rs, g_bs;
   float* dq_acc;  // fused pass: tiled fp32 dQ accumulator, added into
   long long dq_hs, dq_bs;  // its head and batch strides (floats)
+  int n_tasks;             // fused pass: blocks of the launch (rows into the shared tensors)
+  BwdTaskP task[kMaxBwdTasks];
   int B, H, Sq, Sk, causal, grad_mode;
   float scale, scale_log2;
   DevStatus st;
@@ -602,13 +610,21 @@ __global__ void __launch_bounds__(kFuThreads, 1)
   const int lane = static_cast<int>(lane_id());
   constexpr uint32_t kWhere = 4u << 24;
 
-  // Work item and order as in the dK/dV pass (head-major, long rows first).
-  const int nq = (p.Sq + kT - 1) / kT;
-  const int nkt = (p.Sk + kT - 1) / kT;
-  const int bh = static_cast<int>(blockIdx.x / nkt);
-  const int kt = static_cast<int>(blockIdx.x % nkt);
+  // Work item: the task owning this CTA (tasks come longest rows first), then
+  // key tile kt of (b, h) in it, in the dK/dV pass's order (head-major, long
+  // rows first). Row indices below are task-local; q_off / k_off place them
+  // in the shared tensors.
+  int ti = 0;
+  while (ti + 1 < p.n_tasks && static_cast<int>(blockIdx.x) >= p.task[ti + 1].cta0) ++ti;
+  const int Sq = p.task[ti].q_len, Sk = p.task[ti].k_len, causal = p.task[ti].causal;
+  const int q_off = p.task[ti].q_off, k_off = p.task[ti].k_off;
+  const int local = static_cast<int>(blockIdx.x) - p.task[ti].cta0;
+  const int nq = (Sq + kT - 1) / kT;
+  const int nkt = (Sk + kT - 1) / kT;
+  const int bh = local / nkt;
+  const int kt = local % nkt;
   const int b = bh / p.H, h = bh % p.H;
-  const int i0 = p.causal ? kt : 0;
+  const int i0 = causal ? kt : 0;
   const int n = std::max(0, nq - i0);  // query tiles
 
   if (threadIdx.x == 0) {
@@ -630,15 +646,15 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       const int x0 = h * kD;
       const uint64_t pol = l2_policy_evict_last();
       mbar_arrive_expect_tx(&bars->fixed_full, 2 * kTileBytes);
-      load_tile(smem + kFuSmK, &tm_k, &bars->fixed_full, x0, kt * kT, b, pol);
-      load_tile(smem + kFuSmV, &tm_v, &bars->fixed_full, x0, kt * kT, b, pol);
+      load_tile(smem + kFuSmK, &tm_k, &bars->fixed_full, x0, k_off + kt * kT, b, pol);
+      load_tile(smem + kFuSmV, &tm_v, &bars->fixed_full, x0, k_off + kt * kT, b, pol);
       int i = 0;
       bool ok = true;
       for (; i < n && ok; ++i) {
         const int s = i % kKvStages;
         const uint32_t ph = static_cast<uint32_t>(i / kKvStages) & 1u;
         const uint32_t dph = static_cast<uint32_t>(i) & 1u;  // one dO slot
-        const int row = (i0 + i) * kT;
+        const int row = q_off + (i0 + i) * kT;
         ok = mbar_wait(&bars->ring_empty[s], ph ^ 1u, abort_flag, p.st, kWhere | (1u << 16));
         if (!ok) break;
         mbar_arrive_expect_tx(&bars->ring_full[s], kTileBytes);
@@ -734,7 +750,8 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       bool ok = true;
       for (int i = 0; i < n && ok; ++i) {
         const uint32_t ph = static_cast<uint32_t>(i) & 1u;
-        float* tile = p.dq_acc + b * p.dq_bs + h * p.dq_hs + static_cast<long long>(i0 + i) * (kT * kD);
+        float* tile =
+            p.dq_acc + b * p.dq_bs + h * p.dq_hs + static_cast<long long>(q_off / kT + i0 + i) * (kT * kD);
         for (int x = 0; x < 4 && ok; ++x) {  // blocks 0, 1, then 2, 3 reusing the slots
           ok = mbar_wait(&bars->stg_full[x], ph, abort_flag, p.st, kWhere | (14u << 16));
           if (!ok) break;
@@ -755,12 +772,14 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     uint8_t* ds_tile = smem + kFuSmDs;
     uint8_t* stg_row = smem + kFuSmStg + (x & 1) * kDqBlock + row * 128;
     const int j = kt * kT + row;
-    const bool key_ok = j < p.Sk;  // rows past the keys: K is zero-filled there, P must be 0
+    const bool key_ok = j < Sk;  // rows past the block's keys (zero-filled or another block's): P must be 0
     const float c = p.scale_log2;
     auto load_stats = [&](int i, float& l2v, float& dlv) {
       const int q = (i0 + i) * kT + 32 * x + lane;
-      l2v = lse2_of(p, b, h, q);
-      dlv = (q < p.Sq) ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + q) : 0.f;
+      const long long si = b * p.l_bs + h * p.l_hs + q_off + q;
+      const float l = q < Sq ? __ldg(p.lse + si) : -INFINITY;
+      l2v = (l == -INFINITY) ? INFINITY : l * kLog2e;  // hidden or empty rows: P = 0
+      dlv = (q < Sq) ? __ldg(p.delta + si) : 0.f;
     };
     float nl2 = 0.f, ndl = 0.f;
     if (n > 0) load_stats(0, nl2, ndl);
@@ -774,7 +793,7 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       ok = warp_all(mbar_wait(&bars->s_full, ph, abort_flag, p.st, kWhere | (5u << 16)));
       if (!ok) break;
       tc_fence_after();
-      const bool diag = p.causal && (it == kt);
+      const bool diag = causal && (it == kt);
       // Phase 1: P^T, into this warpgroup's own S^T columns (already read by it).
       float pv[32];
       {
@@ -847,9 +866,9 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       mbar_arrive(&bars->stg_full[x]);
     }
     // Epilogue: warpgroups 0/1 write dV columns [0,64)/[64,128), 2/3 write dK (scaled).
-    const bool valid = j < p.Sk;
+    const bool valid = j < Sk;
     const int half = x & 1;
-    const long long off = b * p.g_bs + static_cast<long long>(j) * p.g_rs + h * kD + 64 * half;
+    const long long off = b * p.g_bs + static_cast<long long>(k_off + j) * p.g_rs + h * kD + 64 * half;
     void* gdst = x < 2 ? p.g1 : p.g0;
     const float mul = x < 2 ? 1.f : p.scale;
     const uint32_t tacc = (x < 2 ? tDV : tDK) + lane_off + 64 * half;
@@ -1056,6 +1075,7 @@ Params base_params(const BwdLaunch& a) {
   p.dq_acc = nullptr;
   p.dq_hs = 0;
   p.dq_bs = 0;
+  p.n_tasks = 0;
   p.B = a.B;
   p.H = a.H;
   p.Sq = a.Sq;
@@ -1101,18 +1121,16 @@ int launch_attn_bwd_dkdv(const BwdLaunch& a, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
-int launch_attn_bwd_fused(const BwdLaunch& a, cudaStream_t stream) {
-  if (a.Sk == 0) return 0;
+int launch_attn_bwd_fused(const BwdLaunch& a, const BwdTask* tasks, int n_tasks, int q_rows, int k_rows,
+                          cudaStream_t stream) {
+  if (n_tasks < 1 || n_tasks > kMaxBwdTasks) return -1;
+  if (k_rows == 0 || q_rows == 0) return 0;
   CUtensorMap tk, tv, tq, tdo;
-  memset(&tq, 0, sizeof(tq));
-  memset(&tdo, 0, sizeof(tdo));
   int rc;
-  if ((rc = make_tma_map_bf16(&tk, a.k, a.B, a.Sk, a.H * kD, kT)) != 0) return rc;
-  if ((rc = make_tma_map_bf16(&tv, a.v, a.B, a.Sk, a.H * kD, kT)) != 0) return rc;
-  if (a.Sq > 0) {
-    if ((rc = make_tma_map_bf16(&tq, a.q, a.B, a.Sq, a.H * kD, kT)) != 0) return rc;
-    if ((rc = make_tma_map_bf16(&tdo, a.dO, a.B, a.Sq, a.H * kD, kT)) != 0) return rc;
-  }
+  if ((rc = make_tma_map_bf16(&tk, a.k, a.B, k_rows, a.H * kD, kT)) != 0) return rc;
+  if ((rc = make_tma_map_bf16(&tv, a.v, a.B, k_rows, a.H * kD, kT)) != 0) return rc;
+  if ((rc = make_tma_map_bf16(&tq, a.q, a.B, q_rows, a.H * kD, kT)) != 0) return rc;
+  if ((rc = make_tma_map_bf16(&tdo, a.dO, a.B, q_rows, a.H * kD, kT)) != 0) return rc;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(attn_bwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFuSmem) !=
@@ -1128,8 +1146,16 @@ int launch_attn_bwd_fused(const BwdLaunch& a, cudaStream_t stream) {
   p.dq_acc = static_cast<float*>(a.dq);
   p.dq_hs = a.dq_row_stride;    // tile head stride
   p.dq_bs = a.dq_batch_stride;  // tile batch stride
-  const long long grid = static_cast<long long>((a.Sk + kT - 1) / kT) * a.B * a.H;
-  if (grid > 0x7fffffffLL) return -1;
+  long long grid = 0;
+  p.n_tasks = 0;
+  for (int i = 0; i < n_tasks; ++i) {
+    const BwdTask& t = tasks[i];
+    if (t.q_len == 0 || t.k_len == 0) continue;  // handled by the caller
+    p.task[p.n_tasks++] = {t.q_off, t.q_len, t.k_off, t.k_len, t.causal, static_cast<int>(grid)};
+    grid += static_cast<long long>((t.k_len + kT - 1) / kT) * a.B * a.H;
+    if (grid > 0x7fffffffLL) return -1;
+  }
+  if (grid == 0) return 0;
   attn_bwd_fused_kernel<<<static_cast<unsigned>(grid), kFuThreads, kFuSmem, stream>>>(tk, tv, tq, tdo, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }

@@ -60,10 +60,19 @@ struct BwdLaunch {
 };
 int launch_attn_bwd_dkdv(const BwdLaunch& a, cudaStream_t stream);
 int launch_attn_bwd_dq(const BwdLaunch& a, cudaStream_t stream);
-// One pass: dK/dV as grad_mode says; dQ is added into the tiled fp32
+// One block of a one-pass backward launch (rows relative to the shared tensors;
+// q_off a multiple of 128, the dQ accumulator's tile height).
+struct BwdTask {
+  int q_off, q_len, k_off, k_len, causal;
+};
+constexpr int kMaxBwdTasks = 16;
+// One pass over the tasks in one launch (blocks without queries or keys are
+// skipped): dK/dV as a.grad_mode says; dQ is added into the tiled fp32
 // accumulator a.dq (a.dq_row_stride / a.dq_batch_stride carry its tile head /
-// batch strides in floats).
-int launch_attn_bwd_fused(const BwdLaunch& a, cudaStream_t stream);
+// batch strides in floats). The q/dO views hold q_rows rows, k/v/dk/dv k_rows;
+// tasks are ordered longest rows first and their key ranges do not overlap.
+int launch_attn_bwd_fused(const BwdLaunch& a, const BwdTask* tasks, int n_tasks, int q_rows, int k_rows,
+                          cudaStream_t stream);
 // Tiled fp32 dQ accumulator -> bf16 [B, S, H, D] rows (strides in elements).
 int launch_dq_untile(const float* acc, long long tile_hs, long long tile_bs, void* dq, long long rs, long long bs,
                      int B, int H, int S, cudaStream_t stream);

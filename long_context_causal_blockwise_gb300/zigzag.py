@@ -20,8 +20,9 @@ arithmetic runs in libattn.so kernels:
            (unfused: attn_fwd_ex per task, a bf16 block result, then
            attn_lse_merge)
            end          : lcb_cast_f32_bf16 of the accumulator
-  backward Delta from the final bf16 O (attn_bwd_preprocess), then per task
-           the one-pass backward (attn_bwd_fused_ex) with the rank's FINAL
+  backward Delta from the final bf16 O (attn_bwd_preprocess), then per ring
+           step one grouped one-pass launch (attn_bwd_fused_group) of its P
+           tasks, each with the rank's FINAL
            merged LSE and Delta; dK/dV in fp32, stored at step 0 and
            accumulated after into the owning rank's rows; dQ added into the
            querying rank's tiles of one zeroed tiled accumulator; a cast
@@ -105,9 +106,10 @@ def zigzag_attention_bwd(qz, kz, vz, oz, lse, doz, plan, scale=None, delta=None,
                          fused=True, dq_tiles=None):
     """Backward of the emulated ring; all tensors in zigzag order.
 
-    fused=True runs each task as the one-pass backward, every task adding its
-    dQ into one tiled fp32 accumulator (needs chunks of a multiple of 128
-    rows; otherwise, or with fused=False, the deterministic two-pass form).
+    fused=True runs each ring step as ONE grouped one-pass launch
+    (attn_bwd_group), every task adding its dQ into one tiled fp32
+    accumulator (needs chunks of a multiple of 128 rows); otherwise, or with
+    fused=False, each task runs as the deterministic two-pass form.
     Returns (dq, dk, dv) bf16 [1, S, H, D].
     """
     B, S, H, D = qz.shape
@@ -126,13 +128,20 @@ def zigzag_attention_bwd(qz, kz, vz, oz, lse, doz, plan, scale=None, delta=None,
             dq_tiles = _lib.dq_tiles_zeros(1, H, S, dev)
         else:
             _lib.dq_tiles_zero_(dq_tiles)  # the fused pass only ever adds into dQ
-    for t in plan.order:
-        qs = slice(t["q_off"], t["q_off"] + t["q_len"])
-        ks = slice(t["k_off"], t["k_off"] + t["k_len"])
-        dq_t = dq_tiles[:, :, t["q_off"] // 128:] if fused else dq32[:, qs]
-        _lib.attn_bwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], lse[:, :, qs], delta[:, :, qs], doz[:, qs],
-                         dq_t, dk32[:, ks], dv32[:, ks], bool(t["causal"]), scale,
-                         accumulate=t["step"] > 0, passes="fused" if fused else "both")
+    if fused:
+        # one launch per ring step: the P ranks' tasks of a step own disjoint key rows
+        for step in range(plan.P):
+            tasks = [(t["q_off"], t["q_len"], t["k_off"], t["k_len"], t["causal"])
+                     for t in plan.order if t["step"] == step]
+            _lib.attn_bwd_group(qz, kz, vz, lse, delta, doz, dq_tiles, dk32, dv32, tasks, scale,
+                                accumulate=step > 0)
+    else:
+        for t in plan.order:
+            qs = slice(t["q_off"], t["q_off"] + t["q_len"])
+            ks = slice(t["k_off"], t["k_off"] + t["k_len"])
+            _lib.attn_bwd_ex(qz[:, qs], kz[:, ks], vz[:, ks], lse[:, :, qs], delta[:, :, qs], doz[:, qs],
+                             dq32[:, qs], dk32[:, ks], dv32[:, ks], bool(t["causal"]), scale,
+                             accumulate=t["step"] > 0)
     if fused:
         _lib.dq_untile(dq_tiles, grads[0])
     else:

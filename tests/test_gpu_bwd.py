@@ -240,3 +240,36 @@ def test_monolithic_backward_two_calls_agree():
     torch.cuda.synchronize()
     assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
     assert (g1[0].float() - g2[0].float()).abs().max().item() <= 2 ** -8 * g1[0].float().abs().max().item()
+
+
+def test_grouped_backward_equals_separate_calls():
+    """attn_bwd_group runs several one-pass blocks in one launch: dK and dV
+    equal the per-block attn_bwd_ex(passes="fused") calls bit for bit, dQ (all
+    blocks adding into one tiled accumulator) within fp32 rounding; causal and
+    rectangular blocks, ragged lengths, a block without queries."""
+    B, H, S = 1, 2, 1408
+    scale = D ** -0.5
+    g = torch.Generator(device="cuda").manual_seed(41)
+    q, k, v, do = (torch.randn(B, S, H, D, generator=g, device="cuda").to(torch.bfloat16) for _ in range(4))
+    lse = torch.randn(B, H, S, generator=g, device="cuda") + 6.0  # any statistics do for an equality check
+    delta = torch.randn(B, H, S, generator=g, device="cuda")
+    tasks = [(0, 384, 0, 384, 1),        # causal diagonal block
+             (384, 300, 384, 513, 0),    # rectangular, ragged both ways
+             (768, 640, 1000, 300, 0),   # ragged keys
+             (128, 200, 897, 103, 0),    # overlapping query rows with another block (dQ adds)
+             (0, 0, 1300, 100, 0)]       # no queries: its dK/dV rows are zeroed
+    f32 = lambda: torch.full((B, S, H, D), 3.0, device="cuda")  # noqa: E731
+    t1, dk1, dv1 = lcb.dq_tiles_zeros(B, H, S, "cuda"), f32(), f32()
+    lcb.attn_bwd_group(q, k, v, lse, delta, do, t1, dk1, dv1, tasks, scale, accumulate=False)
+    t2, dk2, dv2 = lcb.dq_tiles_zeros(B, H, S, "cuda"), f32(), f32()
+    for qo, ql, ko, kl, causal in tasks:
+        qs, ks = slice(qo, qo + ql), slice(ko, ko + kl)
+        lcb.attn_bwd_ex(q[:, qs], k[:, ks], v[:, ks], lse[:, :, qs], delta[:, :, qs], do[:, qs],
+                        t2[:, :, qo // 128:], dk2[:, ks], dv2[:, ks], bool(causal), scale, accumulate=False,
+                        passes="fused")
+    torch.cuda.synchronize()
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    assert (dk1[:, 1300:1400] == 0).all() and (dv1[:, 1300:1400] == 0).all()
+    assert (dk1[:, 1400:] == 3.0).all()  # rows of no block are left alone
+    assert torch.allclose(untile_f32(t1, S), untile_f32(t2, S), rtol=1e-5, atol=1e-5)
+    assert torch.isfinite(untile_f32(t1, S)).all()
