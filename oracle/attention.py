@@ -192,8 +192,11 @@ def attn_rows(q, k, v, do, rows, causal, scale):
     """Row-local outputs for a sample of query rows, every batch and head.
 
     O_i, LSE_i, Delta_i and dQ_i depend only on query row i, so a sample of
-    rows is checked exactly without the rest. Returns a dict with
-    o [B,R,H,D], lse [B,H,R], delta [B,H,R] and (when do is given) dq [B,R,H,D].
+    rows is checked exactly without the rest. When causal, a panel of rows
+    only forms the keys up to its last row: the keys after a row are not
+    visible to it, contribute exactly zero, and are left out.
+    Returns a dict with o [B,R,H,D], lse [B,H,R], delta [B,H,R] and (when do
+    is given) dq [B,R,H,D].
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     do = None if do is None else _f64(do)
@@ -209,11 +212,12 @@ def attn_rows(q, k, v, do, rows, causal, scale):
     step = _panel_rows(Sk)
     for b in range(B):
         for h in range(H):
-            kh, vh = k[b, :, h, :], v[b, :, h, :]
             for a0 in range(0, R, step):
                 sel = np.arange(a0, min(R, a0 + step))
                 rr = rows[sel]
-                p, lse = _softmax_rows(scale * (q[b, rr, h, :] @ kh.T), _visible(rr, Sk, causal))
+                nk = min(Sk, int(rr.max()) + 1) if causal else Sk  # keys any row of the panel can see
+                kh, vh = k[b, :nk, h, :], v[b, :nk, h, :]
+                p, lse = _softmax_rows(scale * (q[b, rr, h, :] @ kh.T), _visible(rr, nk, causal))
                 o = p @ vh
                 out["o"][b, sel, h, :] = o
                 out["lse"][b, h, sel] = lse

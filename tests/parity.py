@@ -5,8 +5,9 @@ max-abs 2e-2 and mean-abs 2e-3 of the fp64 oracle; LSE within 1e-3
 absolute; schedule and index work bit-exact.
 """
 
+import multiprocessing as mp
 import os
-from concurrent.futures import ThreadPoolExecutor
+from concurrent.futures import ProcessPoolExecutor, ThreadPoolExecutor
 
 import numpy as np
 
@@ -66,3 +67,66 @@ def map_heads(fn, heads, workers=None):
     workers = workers or min(8, os.cpu_count() or 1)
     with ThreadPoolExecutor(max_workers=max(1, min(workers, len(heads)))) as ex:
         return list(ex.map(fn, heads))
+
+
+def _bf16_bits_to_f64(a):
+    """bf16 values stored as uint16 bit patterns -> fp64 (exact)."""
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _rows_job(path, shape, h, rows, causal, scale):
+    """Worker: oracle.attn_rows on head h of the bf16 q, k, v, dO held in a file."""
+    import oracle
+    arr = np.memmap(path, dtype=np.uint16, mode="r", shape=(4,) + tuple(shape))
+    q, k, v, do = (_bf16_bits_to_f64(arr[i][:, :, h:h + 1, :]) for i in range(4))
+    del arr
+    return oracle.attn_rows(q, k, v, do, rows, causal, scale)
+
+
+def _scratch_dir(nbytes):
+    """/dev/shm when it has room for the inputs, else the temp directory."""
+    import shutil
+    import tempfile
+    for d in ("/dev/shm", tempfile.gettempdir()):
+        try:
+            if os.path.isdir(d) and shutil.disk_usage(d).free > 2 * nbytes:
+                return d
+        except OSError:
+            pass
+    return tempfile.gettempdir()
+
+
+def oracle_rows_by_head(q, k, v, do, rows, causal, scale, workers=None):
+    """oracle.attn_rows for every head of device tensors q, k, v, dO [B, S, H, D]
+    (bf16), one head per task on a pool of spawned processes with one BLAS
+    thread each; the inputs reach the workers through a scratch file (bf16
+    bit patterns). Returns the per-head result dicts in head order."""
+    import tempfile
+    import torch
+    B, S, H, D = q.shape
+    nbytes = 4 * q.numel() * 2
+    fd, path = tempfile.mkstemp(prefix="lcb_oracle_", suffix=".bin", dir=_scratch_dir(nbytes))
+    os.close(fd)
+    try:
+        mm = np.memmap(path, dtype=np.uint16, mode="w+", shape=(4, B, S, H, D))
+        host = torch.from_numpy(mm.view(np.int16))
+        for i, t in enumerate((q, k, v, do)):
+            host[i].copy_(t.contiguous().view(torch.int16))
+        del host
+        mm.flush()
+        del mm
+        workers = workers or min(16, os.cpu_count() or 1, H)
+        saved = {n: os.environ.get(n) for n in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+        os.environ.update({n: "1" for n in saved})  # inherited by the spawned workers
+        try:
+            with ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+                futs = [ex.submit(_rows_job, path, (B, S, H, D), h, rows, causal, scale) for h in range(H)]
+                return [f.result() for f in futs]
+        finally:
+            for n, val in saved.items():
+                if val is None:
+                    os.environ.pop(n, None)
+                else:
+                    os.environ[n] = val
+    finally:
+        os.unlink(path)

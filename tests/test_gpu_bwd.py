@@ -7,7 +7,8 @@ import torch
 import oracle
 import long_context_causal_blockwise_gb300 as lcb
 from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo, sample_rows
-from parity import assert_bf16_close, assert_lse_close, err_stats, head64, map_heads, rows_budget, to64
+from parity import (assert_bf16_close, assert_lse_close, err_stats, head64, map_heads, oracle_rows_by_head,
+                    rows_budget, to64)
 
 pytestmark = pytest.mark.gpu
 D = 128
@@ -116,8 +117,7 @@ def test_config2_sampled_rows_backward():
     dq, dk, dv = lcb.attn_bwd(q, k, v, o, lse, do)
     torch.cuda.synchronize()
     rows = sample_rows(S, rows_budget(4096), seed=1)
-    refs = map_heads(lambda h: oracle.attn_rows(*(head64(t, h) for t in (q, k, v, do)), rows, True, scale),
-                     list(range(H)))
+    refs = oracle_rows_by_head(q, k, v, do, rows, True, scale)
     rows_d = torch.as_tensor(rows, device="cuda")
     assert_bf16_close(to64(o[:, rows_d]), np.concatenate([r["o"] for r in refs], 2), "O C2 sampled")
     assert_lse_close(to64(lse[:, :, rows_d]), np.concatenate([r["lse"] for r in refs], 1))

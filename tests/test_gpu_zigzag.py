@@ -12,7 +12,7 @@ import oracle
 import long_context_causal_blockwise_gb300 as lcb
 from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo, sample_rows
 from long_context_causal_blockwise_gb300.zigzag import ZigzagPlan
-from parity import assert_bf16_close, assert_lse_close, head64, map_heads, rows_budget, to64
+from parity import assert_bf16_close, assert_lse_close, oracle_rows_by_head, rows_budget, to64
 
 pytestmark = pytest.mark.gpu
 D = 128
@@ -55,18 +55,17 @@ def test_small_zigzag_vs_monolithic_and_oracle(S, H, P):
 
 def test_config3_zigzag_131072_p8():
     """B=1, H=32, S=131072, P=8 (16 chunks of 8192): ring result vs monolithic
-    on every element, and vs the oracle on 512 sampled query rows plus every
+    on every element, and vs the oracle on 4096 sampled query rows plus every
     chunk edge, on every head."""
     S, H, P = 131072, 32, 8
     r = _run(S, H, P, seed=0)
     _vs_monolithic(r, "C3")
-    rows = sample_rows(S, rows_budget(512), seed=3)
+    rows = sample_rows(S, rows_budget(4096), seed=3)
     # every chunk edge of the zigzag split: among the most likely places to go wrong
     c = S // (2 * P)
     edges = [e for j in range(1, 2 * P) for e in (j * c - 1, j * c)]
     rows = np.unique(np.concatenate([rows, edges]))
-    refs = map_heads(lambda h: oracle.attn_rows(*(head64(r[n], h) for n in ("q", "k", "v", "do")), rows, True,
-                                                D ** -0.5), list(range(H)))
+    refs = oracle_rows_by_head(r["q"], r["k"], r["v"], r["do"], rows, True, D ** -0.5)
     inv = np.argsort(np.asarray(r["plan"].perm))
     zpos = torch.as_tensor(inv[rows], device="cuda")
     assert_bf16_close(to64(r["oz"][:, zpos]), np.concatenate([x["o"] for x in refs], 2), "O C3 sampled vs oracle")

@@ -242,6 +242,15 @@ def test_sampled_rows_agree_with_full():
     np.testing.assert_allclose(rr["lse"], full["lse"][:, :, rows], atol=1e-13)
     np.testing.assert_allclose(rr["dq"], full["dq"][:, rows], atol=1e-13)
     np.testing.assert_allclose(rr["delta"], full["delta"][:, :, rows], atol=1e-13)
+    # unsorted rows (each panel forms only the keys its rows can see) and a non-causal sample
+    rows2 = np.array([33, 2, 49, 10])
+    rr2 = oracle.attn_rows(q, k, v, do, rows2, True, 0.3)
+    np.testing.assert_allclose(rr2["o"], full["o"][:, rows2], atol=1e-13)
+    np.testing.assert_allclose(rr2["dq"], full["dq"][:, rows2], atol=1e-13)
+    nc = oracle.attn_bwd(q, k, v, do, False, 0.3)
+    rr3 = oracle.attn_rows(q, k, v, do, rows2, False, 0.3)
+    np.testing.assert_allclose(rr3["o"], nc["o"][:, rows2], atol=1e-13)
+    np.testing.assert_allclose(rr3["dq"], nc["dq"][:, rows2], atol=1e-13)
     keys = np.array([0, 5, 49])
     dk, dv = oracle.attn_key_rows(q, k, v, do, keys, [1], True, 0.3)
     np.testing.assert_allclose(dk[:, :, 0], full["dk"][:, keys, 1], atol=1e-12)
