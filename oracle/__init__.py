@@ -23,6 +23,8 @@ Sources (the web pages on EasyContext, cited by title and section):
     (prepare_seq_parallel_inputs).
   * "EasyContext核心技术解析…", §1 "序列并行技术": ring attention, whose ring
     steps compose by merging partial results over disjoint key sets.
+  * "EasyContext核心技术解析…", §3 "RoPE扩展技术": the raised rotary base
+    (rope.py).
 
 Parity pins: every function here is pinned by ``tests/test_oracle.py`` against
 brute force, closed forms, invariants or finite differences; none is
@@ -38,4 +40,5 @@ from .attention import (  # noqa: F401
     attn_key_rows,
 )
 from .merge import lse_merge  # noqa: F401
+from .rope import rope  # noqa: F401
 from .zigzag import zigzag_schedule, zigzag_tasks_pairs, TASK_DIAG, TASK_LOWER, TASK_UPPER  # noqa: F401

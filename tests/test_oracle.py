@@ -469,3 +469,86 @@ def test_planted_mistakes_are_caught(monkeypatch, mutation):
         }[mutation]
         monkeypatch.setattr(oracle, "attn_bwd", _mut_bwd(field, how))
     assert not _pins_pass(), f"planted mistake {mutation} went unnoticed"
+
+
+# ---------------------------------------------------------------- RoPE
+
+def _rope_scalar(x, theta, pos0, inverse=False):
+    """RoPE by plain scalar loops with math.cos / math.sin (tiny inputs only)."""
+    B, S, H, D = x.shape
+    half = D // 2
+    y = np.zeros_like(x, dtype=np.float64)
+    for b in range(B):
+        for i in range(S):
+            for h in range(H):
+                for k in range(half):
+                    a = (pos0 + i) * theta ** (-2.0 * k / D)
+                    if inverse:
+                        a = -a
+                    lo, hi = float(x[b, i, h, k]), float(x[b, i, h, k + half])
+                    y[b, i, h, k] = lo * math.cos(a) - hi * math.sin(a)
+                    y[b, i, h, k + half] = hi * math.cos(a) + lo * math.sin(a)
+    return y
+
+
+def test_rope_matches_scalar_loops():
+    rng = np.random.default_rng(61)
+    x = rng.standard_normal((2, 5, 2, 8))
+    for theta, pos0 in ((1e4, 0), (1e6, 524283), (1e9, 17)):
+        for inv in (False, True):
+            np.testing.assert_allclose(oracle.rope(x, theta, pos0, inv), _rope_scalar(x, theta, pos0, inv),
+                                       atol=1e-12, rtol=0)
+
+
+def test_rope_closed_forms():
+    # D = 4, theta = 100: pair 0 turns by i radians, pair 1 by i / 10; features (0, 2) and (1, 3) pair up
+    x = np.zeros((1, 3, 1, 4))
+    x[0, :, 0, 0] = 1.0   # unit vector in pair 0
+    x[0, :, 0, 3] = 2.0   # second feature of pair 1
+    y = oracle.rope(x, 100.0)
+    for i in range(3):
+        assert y[0, i, 0, 0] == pytest.approx(math.cos(i), abs=1e-15)
+        assert y[0, i, 0, 2] == pytest.approx(math.sin(i), abs=1e-15)
+        assert y[0, i, 0, 1] == pytest.approx(-2.0 * math.sin(i / 10), abs=1e-15)
+        assert y[0, i, 0, 3] == pytest.approx(2.0 * math.cos(i / 10), abs=1e-15)
+    # position 0 is the identity, exactly
+    rng = np.random.default_rng(62)
+    z = rng.standard_normal((1, 1, 3, 16))
+    assert np.array_equal(oracle.rope(z, 1e6), z)
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(63)
+    q = rng.standard_normal((1, 6, 2, 16))
+    k = rng.standard_normal((1, 6, 2, 16))
+    yq = oracle.rope(q, 1e6, 1000)
+    # each pair keeps its length; the inverse undoes the rotation
+    n0 = q[..., :8] ** 2 + q[..., 8:] ** 2
+    n1 = yq[..., :8] ** 2 + yq[..., 8:] ** 2
+    np.testing.assert_allclose(n1, n0, rtol=1e-12)
+    np.testing.assert_allclose(oracle.rope(yq, 1e6, 1000, inverse=True), q, atol=1e-12)
+    # scores depend on positions only through their difference: shifting every position keeps q_i . k_j
+    s1 = np.einsum("bihd,bjhd->bhij", oracle.rope(q, 1e6, 0), oracle.rope(k, 1e6, 0))
+    s2 = np.einsum("bihd,bjhd->bhij", oracle.rope(q, 1e6, 77777), oracle.rope(k, 1e6, 77777))
+    np.testing.assert_allclose(s2, s1, atol=1e-10)
+
+
+def test_planted_rope_mistakes_are_caught():
+    """Interleaved pairs (2k, 2k+1) or the angle's sign flipped must fail the scalar pin."""
+    rng = np.random.default_rng(64)
+    x = rng.standard_normal((1, 4, 1, 8))
+    want = _rope_scalar(x, 1e4, 3)
+
+    def interleaved(x, theta, pos0):
+        y = np.array(x, dtype=np.float64)
+        D = x.shape[3]
+        for i in range(x.shape[1]):
+            for k in range(D // 2):
+                a = (pos0 + i) * theta ** (-2.0 * k / D)
+                lo, hi = x[0, i, 0, 2 * k], x[0, i, 0, 2 * k + 1]
+                y[0, i, 0, 2 * k] = lo * math.cos(a) - hi * math.sin(a)
+                y[0, i, 0, 2 * k + 1] = hi * math.cos(a) + lo * math.sin(a)
+        return y
+    assert not np.allclose(interleaved(x, 1e4, 3), want, atol=1e-6)
+    assert not np.allclose(oracle.rope(x, 1e4, 3, inverse=True), want, atol=1e-6)
+    np.testing.assert_allclose(oracle.rope(x, 1e4, 3), want, atol=1e-12)
