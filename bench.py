@@ -72,6 +72,7 @@ KERNEL_SOURCES = {
     "bwd_dq": ("attn_bwd.cu", "common.cuh", "tmem_ldst.cuh"),
     "dq_untile": ("attn_bwd.cu", "common.cuh"),
     "bwd_preprocess": ("lse_merge.cu", "common.cuh"),
+    "rope": ("rope.cu", "common.cuh"),
 }
 
 
@@ -465,6 +466,46 @@ def run_zigzag(args):
     return 0
 
 
+def run_rope(args):
+    """Times the RoPE kernel (theta = 1e6) on one [1, S, H, 128] bf16 tensor at
+    the long-context stress size S = 524288, H = 32 (4.3 GB), in place, and
+    its inverse; prints one JSON line (not the headline bench line)."""
+    import torch
+
+    import long_context_causal_blockwise_gb300 as lcb
+
+    Sr, Hr, theta = 524288, 32, 1e6
+    dev = torch.device("cuda", 0)
+    lcb.load()
+    g = torch.Generator(device=dev).manual_seed(0)
+    x = torch.randn(1, Sr, Hr, D, generator=g, device=dev).to(torch.bfloat16)
+
+    def timed(fn, steps):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    steps = max(3, min(args.steps, 20))
+    t_fwd = timed(lambda: lcb.rope(x, theta), steps)
+    t_inv = timed(lambda: lcb.rope(x, theta, inverse=True), steps)
+    nbytes = 2 * x.numel() * 2  # read and write every element once
+    _, _, hbm, src = load_peaks()
+    print(json.dumps({
+        "metric": "RoPE (theta=1e6) on one bf16 [1, 524288, 32, 128] tensor, in place",
+        "ms": t_fwd, "ms_inverse": t_inv, "bytes_per_call": nbytes,
+        "gbs": nbytes / t_fwd / 1e6, "gbs_inverse": nbytes / t_inv / 1e6,
+        "frac_of_hbm": nbytes / t_fwd / 1e6 / hbm, "hbm_peak": hbm, "hbm_peak_source": src,
+        "inputs": "larger than L2 (4.3 GB); no flush"}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -474,6 +515,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--H", type=int, default=H, help="heads (profiling of smaller cases only)")
     ap.add_argument("--S", type=int, default=S, help="sequence length (profiling of smaller cases only)")
+    ap.add_argument("--rope", action="store_true",
+                    help="time the RoPE kernel on a [1, 524288, 32, 128] tensor")
     ap.add_argument("--zigzag", action="store_true",
                     help="time the one-device zigzag ring (S=131072, P=8) against monolithic attention")
     ap.add_argument("--print-kernel-hashes", action="store_true",
@@ -481,6 +524,8 @@ def main():
     args = ap.parse_args()
     if args.zigzag:
         return run_zigzag(args)
+    if args.rope:
+        return run_rope(args)
     if args.print_kernel_hashes:
         for k, files in KERNEL_SOURCES.items():
             print(k, kernel_source_hash(files))

@@ -300,6 +300,18 @@ int attn_lse_merge(float* o_acc, float* lse_acc, const void* o_b, const float* l
 int zigzag_schedule(int S, int P, int* perm, lcb_task* tasks);
 
 /*
+ * lcb_rope — rotary position embedding with a raised base, [FA] §3
+ * ("RoPE扩展技术"): y = RoPE(x) on bf16 [B, S, H, D=128] views (x and y share
+ * row/batch strides in elements; 4-byte aligned; x == y allowed). Pair k
+ * couples features k and k + 64 and turns by (pos0 + s) * theta^(-2k/128) at
+ * token s; inverse = 1 turns the other way (the transpose: it maps dQ, dK of
+ * the rotated tensors back to the unrotated ones). Angles are reduced in
+ * fp64, rotated in fp32, rounded to bf16 once.
+ */
+int lcb_rope(const void* x, void* y, int B, int S, int H, int D, double theta, long long pos0, int inverse,
+             long long row_stride, long long batch_stride, void* stream);
+
+/*
  * lcb_permute_rows — row gather/scatter on the device, used to move a
  * [B=1, S, H, D] tensor into zigzag order and back, [ZZ].
  * scatter == 0: dst[t] = src[perm[t]];  scatter == 1: dst[perm[t]] = src[t].

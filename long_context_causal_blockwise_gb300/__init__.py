@@ -6,6 +6,7 @@ Public calls (all run in this library's CUDA kernels):
   attn_fwd, attn_fwd_ex, attn_fwd_group, attn_bwd, attn_bwd_ex, attn_bwd_group, attn_bwd_preprocess, attn_bwd_noalloc,
   dq_tiles_zeros / dq_tiles_zero_ / dq_untile (the one-pass backward's tiled dQ accumulator),
   attn_lse_merge, zigzag_schedule, permute_rows, cast_f32_bf16,
+  rope (rotary position embedding with a raised base, and its inverse),
   zigzag_attention_fwd / zigzag_attention_bwd (the one-device zigzag ring).
 
 The shared library is loaded on first use; importing the package does not
@@ -31,6 +32,7 @@ from ._lib import (  # noqa: F401
     dq_untile,
     load,
     permute_rows,
+    rope,
     selftest_bounded_wait,
     set_wait_limit_ns,
     take_device_status,

@@ -78,6 +78,7 @@ _SIGNATURES = {
     "attn_fwd_group": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _LL, _LL,
                         ctypes.POINTER(LcbFwdTask), _I, _P], _I),
     "zigzag_schedule": ([_I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(LcbTask)], _I),
+    "lcb_rope": ([_P, _P, _I, _I, _I, _I, ctypes.c_double, _LL, _I, _LL, _LL, _P], _I),
     "lcb_permute_rows": ([_P, _P, _P, _I, _LL, _P], _I),
     "lcb_scatter_rows": ([_P, _P, _P, _I, _LL, _P], _I),
     "lcb_cast_f32_bf16": ([_P, _P, _LL, _P], _I),
@@ -427,6 +428,20 @@ def zigzag_schedule(S, P):
     tasks = (LcbTask * (P * P))()
     _check("zigzag_schedule", load().zigzag_schedule(S, P, perm, tasks))
     return list(perm), [{f: getattr(t, f) for f, _ in LcbTask._fields_} for t in tasks]
+
+
+def rope(x, theta, pos0=0, inverse=False, out=None):
+    """RoPE (raised base theta) of a bf16 [B, S, H, 128] view; out=None rotates in place.
+
+    inverse=True applies the transpose (maps dQ/dK of rotated inputs back)."""
+    B, S, H, D = x.shape
+    out = x if out is None else out
+    r, b = _bshd(x, "x")
+    if _bshd(out, "out") != (r, b):
+        raise ValueError("x and out must share strides")
+    _check("lcb_rope", load().lcb_rope(_ptr(x), _ptr(out), B, S, H, D, float(theta), int(pos0), int(inverse), r, b,
+                                       _stream(x)))
+    return out
 
 
 def permute_rows(src, dst, perm_dev, scatter=False):

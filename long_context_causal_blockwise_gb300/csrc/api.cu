@@ -642,6 +642,22 @@ int lcb_cast_f32_bf16(const float* src, void* dst, long long n, void* stream) {
   return finish(launch_cast_f32_bf16(src, dst, n, st), st);
 }
 
+int lcb_rope(const void* x, void* y, int B, int S, int H, int D, double theta, long long pos0, int inverse,
+             long long row_stride, long long batch_stride, void* stream) {
+  if (B < 1 || H < 1 || S < 0) return LCB_ERR_ARG;
+  if (D != kHeadDim) return LCB_ERR_UNSUPPORTED;
+  if (!(theta > 0.0) || !std::isfinite(theta) || (inverse != 0 && inverse != 1)) return LCB_ERR_ARG;
+  if (pos0 < 0 || pos0 + S > (1LL << 40)) return LCB_ERR_ARG;
+  if (S == 0) return LCB_OK;
+  if (!x || !y || (reinterpret_cast<uintptr_t>(x) & 3u) || (reinterpret_cast<uintptr_t>(y) & 3u)) return LCB_ERR_ARG;
+  if (row_stride < static_cast<long long>(H) * D || (row_stride % 2) || batch_stride < 0 || (batch_stride % 2))
+    return LCB_ERR_ARG;
+  RopeFreqs fr;
+  for (int k = 0; k < D / 2; ++k) fr.f[k] = std::pow(theta, -2.0 * k / D);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return finish(launch_rope(x, y, B, S, H, row_stride, batch_stride, pos0, inverse, fr, st), st);
+}
+
 int lcb_selftest_bounded_wait(void* stream) {
   DevStatus st;
   int rc = dev_status(&st);

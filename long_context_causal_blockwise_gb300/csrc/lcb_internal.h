@@ -97,4 +97,12 @@ int launch_wait_selftest(DevStatus st, cudaStream_t stream);
 
 int launch_cast_f32_bf16(const float* src, void* dst, long long n, cudaStream_t stream);
 
+// RoPE frequencies f_k = theta^(-2k/128), k < 64, computed on the host in fp64.
+struct RopeFreqs {
+  double f[64];
+};
+// y = RoPE(x) (inverse: the transpose) on bf16 [B, S, H, 128] views sharing strides.
+int launch_rope(const void* x, void* y, int B, int S, int H, long long row_stride, long long batch_stride,
+                long long pos0, int inverse, const RopeFreqs& fr, cudaStream_t stream);
+
 }  // namespace lcb
