@@ -25,6 +25,8 @@ Sources (the web pages on EasyContext, cited by title and section):
     steps compose by merging partial results over disjoint key sets.
   * "EasyContext核心技术解析…", §3 "RoPE扩展技术": the raised rotary base
     (rope.py).
+  * "EasyContext内存优化秘籍DeepSpeed Zero3卸载策略详解", §进阶优化与其他技术结合:
+    the fused cross-entropy loss with an in-place backward (cross_entropy.py).
 
 Parity pins: every function here is pinned by ``tests/test_oracle.py`` against
 brute force, closed forms, invariants or finite differences; none is
@@ -41,4 +43,5 @@ from .attention import (  # noqa: F401
 )
 from .merge import lse_merge  # noqa: F401
 from .rope import rope  # noqa: F401
+from .cross_entropy import ce_fwd, ce_grad, ce_lse  # noqa: F401
 from .zigzag import zigzag_schedule, zigzag_tasks_pairs, TASK_DIAG, TASK_LOWER, TASK_UPPER  # noqa: F401

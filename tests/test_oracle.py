@@ -552,3 +552,70 @@ def test_planted_rope_mistakes_are_caught():
     assert not np.allclose(interleaved(x, 1e4, 3), want, atol=1e-6)
     assert not np.allclose(oracle.rope(x, 1e4, 3, inverse=True), want, atol=1e-6)
     np.testing.assert_allclose(oracle.rope(x, 1e4, 3), want, atol=1e-12)
+
+
+# ---------------------------------------------------------------- cross-entropy
+
+def test_ce_matches_scalar_loops():
+    rng = np.random.default_rng(71)
+    x = rng.standard_normal((4, 7)) * 3
+    y = np.array([0, 6, -100, 3])
+    loss, lse = oracle.ce_fwd(x, y)
+    g = np.array([1.0, 0.5, 2.0, -1.0])
+    grad = oracle.ce_grad(x, y, g)
+    for i in range(4):
+        z = sum(math.exp(v) for v in x[i])
+        assert lse[i] == pytest.approx(math.log(z), abs=1e-12)
+        if y[i] == -100:
+            assert loss[i] == 0.0 and (grad[i] == 0).all()
+            continue
+        assert loss[i] == pytest.approx(-math.log(math.exp(x[i, y[i]]) / z), abs=1e-12)
+        for j in range(7):
+            want = g[i] * (math.exp(x[i, j]) / z - (1.0 if j == y[i] else 0.0))
+            assert grad[i, j] == pytest.approx(want, abs=1e-12)
+
+
+def test_ce_closed_forms_and_invariants():
+    V = 1000
+    x = np.zeros((3, V))
+    loss, lse = oracle.ce_fwd(x, [0, 5, 999])
+    np.testing.assert_allclose(loss, np.log(V), rtol=1e-14)          # uniform logits: loss = ln V
+    x[1, 5] = 80.0
+    loss, _ = oracle.ce_fwd(x, [0, 5, 999])
+    assert loss[1] < 1e-30                                            # a dominant correct logit: loss -> 0
+    rng = np.random.default_rng(72)
+    z = rng.standard_normal((5, 50)) * 4
+    y = rng.integers(0, 50, 5)
+    grad = oracle.ce_grad(z, y, 1.0)
+    np.testing.assert_allclose(grad.sum(axis=1), 0.0, atol=1e-13)     # rows of (softmax - onehot) sum to 0
+    l1, _ = oracle.ce_fwd(z, y)
+    l2, _ = oracle.ce_fwd(z + 123.0, y)                                # a constant per row changes nothing
+    np.testing.assert_allclose(l2, l1, atol=1e-11)
+    np.testing.assert_allclose(oracle.ce_grad(z + 123.0, y, 1.0), grad, atol=1e-13)
+
+
+def test_ce_gradient_by_finite_differences():
+    rng = np.random.default_rng(73)
+    x = rng.standard_normal((3, 9))
+    y = np.array([2, -100, 8])
+    g = np.array([0.7, 1.3, -0.4])
+    grad = oracle.ce_grad(x, y, g)
+    h = 1e-6
+    for i in range(3):
+        for j in range(9):
+            xp, xm = x.copy(), x.copy()
+            xp[i, j] += h
+            xm[i, j] -= h
+            fd = (np.dot(g, oracle.ce_fwd(xp, y)[0]) - np.dot(g, oracle.ce_fwd(xm, y)[0])) / (2 * h)
+            assert grad[i, j] == pytest.approx(fd, abs=1e-8)
+
+
+def test_planted_ce_mistakes_are_caught():
+    """A gradient without the one-hot term, or a loss with the wrong sign, must fail."""
+    rng = np.random.default_rng(74)
+    x = rng.standard_normal((2, 6))
+    y = np.array([1, 4])
+    p = np.exp(x - oracle.ce_lse(x)[:, None])
+    assert not np.allclose(p, oracle.ce_grad(x, y, 1.0), atol=1e-3)
+    loss, lse = oracle.ce_fwd(x, y)
+    assert not np.allclose(x[[0, 1], y] - lse, loss, atol=1e-3)
