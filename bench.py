@@ -73,6 +73,7 @@ KERNEL_SOURCES = {
     "dq_untile": ("attn_bwd.cu", "common.cuh"),
     "bwd_preprocess": ("lse_merge.cu", "common.cuh"),
     "rope": ("rope.cu", "common.cuh"),
+    "cross_entropy": ("cross_entropy.cu", "common.cuh"),
 }
 
 
@@ -506,6 +507,51 @@ def run_rope(args):
     return 0
 
 
+def run_ce(args):
+    """Times the cross-entropy loss head, forward and in-place backward in one
+    pass, on Llama-2's vocabulary (V = 32000) over a 32768-token sequence
+    (2.1 GB of bf16 logits); prints one JSON line (not the headline bench line)."""
+    import torch
+
+    import long_context_causal_blockwise_gb300 as lcb
+
+    N, V = 32768, 32000
+    dev = torch.device("cuda", 0)
+    lcb.load()
+    g = torch.Generator(device=dev).manual_seed(0)
+    x = (torch.randn(N, V, generator=g, device=dev) * 3).to(torch.bfloat16)
+    y = torch.randint(0, V, (N,), generator=g, device=dev)
+    loss = torch.empty(N, device=dev)
+    lse = torch.empty(N, device=dev)
+
+    def timed(fn, steps):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    steps = max(3, min(args.steps, 20))
+    t_fwd = timed(lambda: lcb.cross_entropy(x, y, mode="fwd", loss=loss, lse=lse), steps)
+    t_fb = timed(lambda: lcb.cross_entropy(x, y, mode="fwd_bwd", loss=loss, lse=lse), steps)
+    nb_fwd = N * V * 2 + N * (8 + 8)
+    nb_fb = 2 * N * V * 2 + N * (8 + 8)
+    _, _, hbm, src = load_peaks()
+    print(json.dumps({
+        "metric": "cross-entropy loss head, V=32000, N=32768 tokens, bf16 logits",
+        "fwd_bwd_ms": t_fb, "fwd_ms": t_fwd, "tokens_per_s_fwd_bwd": N / t_fb * 1e3,
+        "fwd_bwd_gbs": nb_fb / t_fb / 1e6, "fwd_gbs": nb_fwd / t_fwd / 1e6,
+        "fwd_bwd_frac_of_hbm": nb_fb / t_fb / 1e6 / hbm, "fwd_frac_of_hbm": nb_fwd / t_fwd / 1e6 / hbm,
+        "hbm_peak": hbm, "hbm_peak_source": src,
+        "inputs": "larger than L2 (2.1 GB of logits); no flush"}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -515,6 +561,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--H", type=int, default=H, help="heads (profiling of smaller cases only)")
     ap.add_argument("--S", type=int, default=S, help="sequence length (profiling of smaller cases only)")
+    ap.add_argument("--ce", action="store_true",
+                    help="time the cross-entropy loss head (V=32000, 32768 tokens)")
     ap.add_argument("--rope", action="store_true",
                     help="time the RoPE kernel on a [1, 524288, 32, 128] tensor")
     ap.add_argument("--zigzag", action="store_true",
@@ -526,6 +574,8 @@ def main():
         return run_zigzag(args)
     if args.rope:
         return run_rope(args)
+    if args.ce:
+        return run_ce(args)
     if args.print_kernel_hashes:
         for k, files in KERNEL_SOURCES.items():
             print(k, kernel_source_hash(files))

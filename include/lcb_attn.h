@@ -299,6 +299,28 @@ int attn_lse_merge(float* o_acc, float* lse_acc, const void* o_b, const float* l
  */
 int zigzag_schedule(int S, int P, int* perm, lcb_task* tasks);
 
+/* lcb_cross_entropy modes. */
+#define LCB_CE_FWD 0     /* loss and LSE; logits read only */
+#define LCB_CE_FWD_BWD 1 /* loss and LSE, and the gradient written over the logits: one read, one write */
+#define LCB_CE_BWD 2     /* the gradient over the logits from a given LSE (a previous LCB_CE_FWD) */
+
+/*
+ * lcb_cross_entropy — the cross-entropy loss head with an in-place backward,
+ * [ZO] §进阶优化与其他技术结合 (Flash Attention's fused CrossEntropyLoss with
+ * inplace_backward=True). Per row i of logits x (bf16 [N, V], row stride in
+ * elements, 2-byte aligned) with label y_i (int64 [N], DEVICE):
+ *   lse[i]  = ln sum_j exp(x_ij)                       (fp32 [N], DEVICE)
+ *   loss[i] = lse[i] - x_{i,y_i}                       (fp32 [N], DEVICE; NULL: not written)
+ *   x_ij   <- dloss[i] * (exp(x_ij - lse[i]) - [j == y_i])   (bf16, in place)
+ * dloss: fp32 [N] DEVICE, NULL meaning 1 for every row. A row whose label is
+ * ignore_index gets loss 0 and a zero gradient; a label outside [0, V)
+ * otherwise gives loss NaN (and no one-hot term). Each row is staged whole in
+ * shared memory: V * 2 bytes must fit next to a few hundred bytes of
+ * bookkeeping in 227 KB (V <= 115000), else LCB_ERR_UNSUPPORTED.
+ */
+int lcb_cross_entropy(void* logits, const long long* labels, float* loss, float* lse, const float* dloss, int N,
+                      int V, long long row_stride, int ignore_index, int mode, void* stream);
+
 /*
  * lcb_rope — rotary position embedding with a raised base, [FA] §3
  * ("RoPE扩展技术"): y = RoPE(x) on bf16 [B, S, H, D=128] views (x and y share

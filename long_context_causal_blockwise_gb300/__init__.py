@@ -7,6 +7,7 @@ Public calls (all run in this library's CUDA kernels):
   dq_tiles_zeros / dq_tiles_zero_ / dq_untile (the one-pass backward's tiled dQ accumulator),
   attn_lse_merge, zigzag_schedule, permute_rows, cast_f32_bf16,
   rope (rotary position embedding with a raised base, and its inverse),
+  cross_entropy (the loss head with an in-place backward),
   zigzag_attention_fwd / zigzag_attention_bwd (the one-device zigzag ring).
 
 The shared library is loaded on first use; importing the package does not
@@ -27,6 +28,7 @@ from ._lib import (  # noqa: F401
     attn_fwd_group,
     attn_lse_merge,
     cast_f32_bf16,
+    cross_entropy,
     dq_tiles_zero_,
     dq_tiles_zeros,
     dq_untile,

@@ -78,6 +78,7 @@ _SIGNATURES = {
     "attn_fwd_group": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _LL, _LL,
                         ctypes.POINTER(LcbFwdTask), _I, _P], _I),
     "zigzag_schedule": ([_I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(LcbTask)], _I),
+    "lcb_cross_entropy": ([_P, _P, _P, _P, _P, _I, _I, _LL, _I, _I, _P], _I),
     "lcb_rope": ([_P, _P, _I, _I, _I, _I, ctypes.c_double, _LL, _I, _LL, _LL, _P], _I),
     "lcb_permute_rows": ([_P, _P, _P, _I, _LL, _P], _I),
     "lcb_scatter_rows": ([_P, _P, _P, _I, _LL, _P], _I),
@@ -428,6 +429,37 @@ def zigzag_schedule(S, P):
     tasks = (LcbTask * (P * P))()
     _check("zigzag_schedule", load().zigzag_schedule(S, P, perm, tasks))
     return list(perm), [{f: getattr(t, f) for f, _ in LcbTask._fields_} for t in tasks]
+
+
+_CE_MODES = {"fwd": 0, "fwd_bwd": 1, "bwd": 2}
+
+
+def cross_entropy(logits, labels, ignore_index=-100, mode="fwd_bwd", dloss=None, lse=None, loss=None):
+    """Cross-entropy of bf16 logits [N, V] against int64 labels [N].
+
+    mode "fwd": returns (loss, lse); "fwd_bwd": also overwrites logits with
+    dloss_i * (softmax - onehot) (dloss None: 1 per row); "bwd": the gradient
+    alone from a given lse. Returns (loss, lse)."""
+    if logits.dim() != 2 or logits.dtype != torch.bfloat16 or logits.stride(1) != 1:
+        raise ValueError("logits must be a bf16 [N, V] view with unit column stride")
+    N, V = logits.shape
+    if labels.dtype != torch.int64 or labels.shape != (N,) or not labels.is_contiguous():
+        raise ValueError("labels must be a contiguous int64 [N] tensor")
+    dev = logits.device
+    if mode == "bwd":
+        if lse is None:
+            raise ValueError("mode 'bwd' needs the lse of a previous forward")
+    else:
+        lse = torch.empty(N, dtype=torch.float32, device=dev) if lse is None else lse
+        loss = torch.empty(N, dtype=torch.float32, device=dev) if loss is None else loss
+    for t, n in ((lse, "lse"), (loss, "loss"), (dloss, "dloss")):
+        if t is not None and (t.dtype != torch.float32 or t.shape != (N,) or not t.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous fp32 [N] tensor")
+    _check("lcb_cross_entropy", load().lcb_cross_entropy(
+        _ptr(logits), _ptr(labels), None if loss is None else _ptr(loss), _ptr(lse),
+        None if dloss is None else _ptr(dloss), N, V, logits.stride(0), int(ignore_index), _CE_MODES[mode],
+        _stream(logits)))
+    return loss, lse
 
 
 def rope(x, theta, pos0=0, inverse=False, out=None):
