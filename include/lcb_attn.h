@@ -16,6 +16,14 @@
  *        (zigzag_ring_attn) and §训练循环核心逻辑 (prepare_seq_parallel_inputs
  *        splits each sequence into rank-local pieces).
  *  [FULL] "EasyContext：用最少资源扩展大模型至百万Token": full attention.
+ *  [ZO]  "EasyContext内存优化秘籍DeepSpeed Zero3卸载策略详解",
+ *        §进阶优化与其他技术结合 (the fused cross-entropy loss with an
+ *        in-place backward; the raised RoPE base) and §训练脚本配置
+ *        (--rope-theta 1000000).
+ *
+ * Beyond attention: the rotary position embedding with a raised base that
+ * long-context training puts on Q and K ([FA] §3 "RoPE扩展技术", [ZO]) and
+ * the cross-entropy loss head ([ZO]).
  *
  * Conventions shared by every entry point
  *  - Tensors Q, K, V, O, dO, dQ, dK, dV are [B, S, H, D] (token-major, heads
@@ -29,8 +37,10 @@
  *  - stream is a cudaStream_t (NULL = legacy default stream). Every compute
  *    call only enqueues work and returns; results are ready when the stream
  *    reaches that point.
- *  - Device pointers must be 16-byte aligned and strides multiples of 8
- *    elements (16 bytes), as required by the tensor-memory-access (TMA) unit.
+ *  - Device pointers of the attention calls must be 16-byte aligned and
+ *    strides multiples of 8 elements (16 bytes), as required by the
+ *    tensor-memory-access (TMA) unit; lcb_rope and lcb_cross_entropy state
+ *    their own, weaker rules.
  *  - Return value: LCB_OK or a negative LCB_ERR_* code; nothing is launched on
  *    an argument error. With the environment variable LCB_CHECKED=1 every call
  *    synchronises its stream and reports LCB_ERR_TIMEOUT if a kernel's
