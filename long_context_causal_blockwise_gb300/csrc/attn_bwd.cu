@@ -184,37 +184,41 @@ __device__ __forceinline__ void fixed_to_tmem(const __nv_bfloat16* base, long lo
 
 // D = A x B^T over K = 128, A and B 128-row K-major tiles in shared memory.
 __device__ __forceinline__ void mma_ss_tile(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc, bool accumulate) {
+  const uint64_t da = sdesc_sw128(a, 16, 1024), db = sdesc_sw128(b, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t off = (kk >> 2) * kColHalf + (kk & 3) * 32;
-    mma_ss(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), idesc, (accumulate || kk > 0));
+    mma_ss(d, sdesc_advance(da, off), sdesc_advance(db, off), idesc, (accumulate || kk > 0));
   }
 }
 
 // D = A x B^T over K = 128, A in TMEM (64 columns of bf16 pairs), B a K-major tile.
 __device__ __forceinline__ void mma_ts_tile(uint32_t d, uint32_t a_tmem, uint32_t b, uint32_t idesc) {
+  const uint64_t db = sdesc_sw128(b, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t off = (kk >> 2) * kColHalf + (kk & 3) * 32;
-    mma_ts(d, a_tmem + kk * 8, sdesc_sw128(b + off, 16, 1024), idesc, kk > 0);
+    mma_ts(d, a_tmem + kk * 8, sdesc_advance(db, off), idesc, kk > 0);
   }
 }
 
 // D (+)= A x B over K = 128, A a K-major tile in shared memory, B an MN-major tile [K rows][N = 128].
 __device__ __forceinline__ void mma_ss_tile_mn(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc, bool accumulate) {
+  const uint64_t da = sdesc_sw128(a, 16, 1024), db = sdesc_sw128(b, kColHalf, 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t a_off = (kk >> 2) * kColHalf + (kk & 3) * 32;
-    mma_ss(d, sdesc_sw128(a + a_off, 16, 1024), sdesc_sw128(b + kk * 2048, kColHalf, 1024), idesc,
+    mma_ss(d, sdesc_advance(da, a_off), sdesc_advance(db, kk * 2048), idesc,
            (accumulate || kk > 0));
   }
 }
 
 // D = A x B over K = 128, A and B MN-major tiles [K rows][M or N = 128] (A^T and B as stored).
 __device__ __forceinline__ void mma_ss_tile_mnmn(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc) {
+  const uint64_t da = sdesc_sw128(a, kColHalf, 1024), db = sdesc_sw128(b, kColHalf, 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    mma_ss(d, sdesc_sw128(a + kk * 2048, kColHalf, 1024), sdesc_sw128(b + kk * 2048, kColHalf, 1024), idesc,
+    mma_ss(d, sdesc_advance(da, kk * 2048), sdesc_advance(db, kk * 2048), idesc,
            kk > 0);
   }
 }
@@ -437,11 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bars->pt_full, ph, abort_flag, p.st, kWhere | (4u << 16));
         if (!ok) break;
         tc_fence_after();
+        const uint64_t ddo = sdesc_sw128(do_slot(i), kColHalf, 1024);
         // dV += P^T(i) dO_i; P^T K-step kk (queries 16kk..16kk+15) sits at columns 32(kk/2) + 8(kk%2)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t a = tS + 32 * (kk >> 1) + 8 * (kk & 1);
-          mma_ts(tDV, a, sdesc_sw128(do_slot(i) + kk * 2048, kColHalf, 1024), id_g, (i > 0 || kk > 0));
+          mma_ts(tDV, a, sdesc_advance(ddo, kk * 2048), id_g, (i > 0 || kk > 0));
         }
         tc_commit(&bars->do_empty[i % kKvStages]);
         if (i + 1 < n) {
@@ -708,11 +713,12 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         ok = mbar_wait(&bars->pt_full, ph, abort_flag, p.st, kWhere | (4u << 16));
         if (!ok) break;
         tc_fence_after();
+        const uint64_t ddo = sdesc_sw128(sDo, kColHalf, 1024);
         // dV += P^T(i) dO_i; P^T K-step kk (queries 16kk..16kk+15) sits at columns 32(kk/2) + 8(kk%2)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t a = tS + 32 * (kk >> 1) + 8 * (kk & 1);
-          mma_ts(tDV, a, sdesc_sw128(sDo + kk * 2048, kColHalf, 1024), id_g, (i > 0 || kk > 0));
+          mma_ts(tDV, a, sdesc_advance(ddo, kk * 2048), id_g, (i > 0 || kk > 0));
         }
         tc_commit(&bars->do_empty[0]);  // the dO slot may take dO(i+1)
         if (i + 1 < n) {

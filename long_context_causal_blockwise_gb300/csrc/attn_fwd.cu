@@ -203,19 +203,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
       const uint32_t idesc_pv = idesc_bf16(kBM, kD, false, true);
       auto issue_qk = [&](int t, int slot) {
-        const uint32_t qa = sbase + kSmQ + t * kTileBytes;
-        const uint32_t kb = sbase + kSmKV + slot * kTileBytes;
+        const uint64_t qa = sdesc_sw128(sbase + kSmQ + t * kTileBytes, 16, 1024);
+        const uint64_t kb = sdesc_sw128(sbase + kSmKV + slot * kTileBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(tbase + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+          mma_ss(tbase + t * 128, sdesc_advance(qa, off), sdesc_advance(kb, off), idesc_qk, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t vb = sbase + kSmKV + slot * kTileBytes;
+        const uint64_t vb = sdesc_sw128(sbase + kSmKV + slot * kTileBytes, kHalfBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          mma_ts(tbase + 256 + t * 128, tbase + t * 128 + kk * 8, sdesc_sw128(vb + kk * 2048, kHalfBytes, 1024), idesc_pv, (acc || kk > 0));
+          mma_ts(tbase + 256 + t * 128, tbase + t * 128 + kk * 8, sdesc_advance(vb, kk * 2048), idesc_pv,
+                 (acc || kk > 0));
         }
       };
       bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.st, kWhere | (2u << 16));

@@ -233,6 +233,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The descriptor of an operand `bytes` further on (a multiple of 16): only the
+// start-address field changes, and shared-memory addresses stay below 256 KB,
+// so the field never carries into the next. One add instead of rebuilding.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format (1 = bf16)
 //   bit 15 A major (0 = K-major); bit 16 B major (1 = MN-major)
