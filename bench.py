@@ -3,8 +3,9 @@
 
 Workload: one Llama-2-7B attention layer, B=1, H=32, S=32768, D=128, causal,
 bf16 Q/K/V/dO drawn i.i.d. N(0,1) from a seed (synthetic, no dataset), scale
-1/sqrt(128). A step is the whole hot path once: attn_fwd, the Delta
-preprocess, the dK/dV pass and the dQ pass (all libattn.so kernels).
+1/sqrt(128). A step is the whole hot path once: attn_fwd, then the calls
+attn_bwd makes (the Delta preprocess, zeroing of the tiled dQ accumulator, the
+one-pass backward, dQ to bf16), all in libattn.so.
 
 FLOP convention (causal, half of the S x S pairs): forward 2*B*H*S^2*D,
 backward 2.5 x forward, step 7*B*H*S^2*D.
@@ -44,6 +45,23 @@ def _set_shape(h, s):
     H, S = h, s
     WORKLOAD = f"causal fwd+bwd B1 H{h} S{s} D128 (profiling case)"
     L2_NOTE = f"q,k,v,dO are {s * h * D * 2 / 1e6:.0f} MB each"
+
+
+def max_over_ranks(x, world, device):
+    """The largest value of a per-rank float over all ranks (every rank gets it)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flop_per_rank_step, steps, t_max):
+    """Whole-job throughput: every rank's FLOP over the slowest rank's time."""
+    return world * flop_per_rank_step * steps / t_max / 1e12
 
 
 def step_flop(b, h, s, d):
@@ -269,11 +287,7 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     clocks = sampler.stop()
     elapsed = t_start.elapsed_time(t_end) / 1e3
-    t_max = elapsed
-    if world > 1:
-        tt = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = max_over_ranks(elapsed, world, dev)
     per = {n: [] for n in names}
     for evs in events:
         for j, n in enumerate(names):
@@ -308,11 +322,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_t = e0.elapsed_time(e1) / 1e3 / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_t], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_t = float(tt.item())
+    e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3 / e2e_steps, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v, do))
     d2h = sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv))
     # the e2e outputs must equal the device-resident run's: O, dK, dV bit for bit; dQ (fp32
@@ -326,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
 
     sus, burst, hbm, src = load_peaks()
     flop = step_flop(B, H, S, D)
-    value = world * flop * args.steps / t_max / 1e12
+    value = whole_job_tflops(world, flop, args.steps, t_max)
     ms = 1e3 * t_max / args.steps
     pairs = B * H * S * S / 2.0  # causal (query, key) pairs, the R5 convention
     tiles_bytes = B * H * ((S + 127) // 128) * 128 * D * 4
@@ -375,7 +385,7 @@ def run_ours(args, rank, world, local_rank):
         "bwd_frac_of_peak": 2.5 * fwd_flop(B, H, S, D) / bwd_t / 1e12 / sus,
         "kernels": kernels,
         "roofline": roof,
-        "e2e": {"value": world * flop / e2e_t / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_tflops(world, flop, 1, e2e_t), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_t, "matches_device_run": same},
         "gpu_launches": 4 * args.steps,  # attn_fwd, bwd_preprocess, bwd_fused, dq_untile (dq_zero is a memset)
         "clocks": clocks,
