@@ -436,14 +436,7 @@ int attn_bwd_fused_group(const void* q, const void* k, const void* v, const floa
   const int Sq = q_rows, Sk = k_rows, causal = 0;  // shared tensors; causality is per task
   const long long HD = static_cast<long long>(H) * kHeadDim;
   const long long dq_row_stride = HD, dq_batch_stride = HD * Sq;
-  BwdLaunch a;
-  int rc = prep_bwd(&a, LCB_BWD_EX_ARGS);
-  if (rc != LCB_OK) return rc;
-  a.dq_row_stride = dq_tile_head_stride;
-  a.dq_batch_stride = dq_tile_batch_stride;
-  BwdTask order[kMaxBwdTasks];
-  int m = 0;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (q_rows < 0 || k_rows < 0) return LCB_ERR_ARG;
   for (int i = 0; i < n_tasks; ++i) {
     const lcb_bwd_task& x = tasks[i];
     if (x.causal != 0 && x.causal != 1) return LCB_ERR_ARG;
@@ -457,6 +450,14 @@ int attn_bwd_fused_group(const void* q, const void* k, const void* v, const floa
         return LCB_ERR_ARG;
     }
   }
+  BwdLaunch a;
+  int rc = prep_bwd(&a, LCB_BWD_EX_ARGS);
+  if (rc != LCB_OK) return rc;
+  a.dq_row_stride = dq_tile_head_stride;
+  a.dq_batch_stride = dq_tile_batch_stride;
+  BwdTask order[kMaxBwdTasks];
+  int m = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   for (int i = 0; i < n_tasks; ++i) {
     const lcb_bwd_task& x = tasks[i];
     if (x.k_len == 0) continue;

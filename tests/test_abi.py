@@ -101,6 +101,42 @@ def test_fwd_group_argument_errors_need_no_gpu(lib):
     assert call([]) == _lib.LCB_OK                                                           # nothing to do
 
 
+def test_bwd_group_rope_ce_argument_errors_need_no_gpu(lib):
+    """The newer entry points reject bad arguments before any CUDA call."""
+    nul = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(1 << 20)
+
+    def bwd(tasks, n=None, tile_hs=16384 * 8):
+        arr = (_lib.LcbBwdTask * max(1, len(tasks)))(*[_lib.LcbBwdTask(*t) for t in tasks])
+        return lib.attn_bwd_fused_group(fake, fake, fake, fake, fake, fake, fake, fake, fake, 1, 2, 1024, 1024, 128,
+                                        0.1, 256, 0, 256, 0, 1024, 2048, _lib.LCB_GRAD_BF16, tile_hs, 0, 256, 0, arr,
+                                        len(tasks) if n is None else n, nul)
+    assert bwd([(64, 128, 0, 128, 0)]) == _lib.LCB_ERR_ARG                             # q_off not on a dQ tile
+    assert bwd([(0, 128, 0, 256, 0), (128, 128, 128, 256, 0)]) == _lib.LCB_ERR_ARG     # key ranges overlap
+    assert bwd([(0, 128, 900, 256, 0)]) == _lib.LCB_ERR_ARG                            # keys past k_rows
+    assert bwd([(0, 128, 0, 256, 1)]) == _lib.LCB_ERR_UNSUPPORTED                      # causal needs a square
+    assert bwd([(0, 128, 0, 128, 0)], tile_hs=3) == _lib.LCB_ERR_ARG                   # tile stride not 16-byte
+    assert bwd([(0, 128, 0, 128, 0)], n=17) == _lib.LCB_ERR_ARG                        # at most 16 tasks
+    # RoPE: D, theta, inverse flag, alignment, row stride
+    assert lib.lcb_rope(fake, fake, 1, 8, 2, 64, 1e6, 0, 0, 256, 0, nul) == _lib.LCB_ERR_UNSUPPORTED
+    assert lib.lcb_rope(fake, fake, 1, 8, 2, 128, -1.0, 0, 0, 256, 0, nul) == _lib.LCB_ERR_ARG
+    assert lib.lcb_rope(fake, fake, 1, 8, 2, 128, 1e6, 0, 2, 256, 0, nul) == _lib.LCB_ERR_ARG
+    assert lib.lcb_rope(ctypes.c_void_p(2), fake, 1, 8, 2, 128, 1e6, 0, 0, 256, 0, nul) == _lib.LCB_ERR_ARG
+    assert lib.lcb_rope(fake, fake, 1, 8, 2, 128, 1e6, 0, 0, 128, 0, nul) == _lib.LCB_ERR_ARG
+    assert lib.lcb_rope(fake, fake, 1, 0, 2, 128, 1e6, 0, 0, 256, 0, nul) == _lib.LCB_OK
+    # cross-entropy: mode, row stride, vocabulary too large for one staged row, null pointers, empty
+    assert lib.lcb_cross_entropy(fake, fake, fake, fake, nul, 4, 100, 100, -100, 3, nul) == _lib.LCB_ERR_UNSUPPORTED
+    assert lib.lcb_cross_entropy(fake, fake, fake, fake, nul, 4, 100, 99, -100, 0, nul) == _lib.LCB_ERR_ARG
+    assert lib.lcb_cross_entropy(fake, fake, fake, fake, nul, 4, 200000, 200000, -100, 0,
+                                 nul) == _lib.LCB_ERR_UNSUPPORTED
+    assert lib.lcb_cross_entropy(fake, nul, fake, fake, nul, 4, 100, 100, -100, 1, nul) == _lib.LCB_ERR_ARG
+    assert lib.lcb_cross_entropy(fake, fake, fake, fake, nul, 0, 100, 100, -100, 1, nul) == _lib.LCB_OK
+    # dQ accumulator helpers
+    assert lib.lcb_dq_untile(fake, 3, 0, fake, 256, 0, 1, 2, 16, nul) == _lib.LCB_ERR_ARG
+    assert lib.lcb_dq_tiles_zero(ctypes.c_void_p(4), 16, nul) == _lib.LCB_ERR_ARG
+    assert lib.attn_bwd_workspace_bytes(1, 2, 300, 128) == 2 * 300 * 4 + 1 * 2 * 3 * 16384 * 4 + 256 - (2 * 300 * 4) % 256
+
+
 @pytest.mark.parametrize("S,P", [(8, 2), (16, 1), (48, 3), (256, 4), (256, 8), (131072, 8), (524288, 8)])
 def test_zigzag_schedule_matches_oracle_bit_exact(lib, S, P):
     perm, tasks = _lib.zigzag_schedule(S, P)
