@@ -536,7 +536,6 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   float* delta = static_cast<float*>(workspace);
   float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes(B, H, S));
   const long long tile_hs = dq_tiles(S) * kDqTileFloats, tile_bs = tile_hs * H;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = attn_bwd_preprocess(o, dO, delta, B, H, S, D, rs, bs, S, static_cast<long long>(H) * S, stream);
   if (rc != LCB_OK) return rc;
   if ((rc = lcb_dq_tiles_zero(dq_acc, tile_bs * B, stream)) != LCB_OK) return rc;

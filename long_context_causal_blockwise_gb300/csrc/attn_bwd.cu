@@ -7,9 +7,15 @@
 // dS_ij = P_ij (dP_ij - Delta_i):
 //   dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j.
 //
-// Two passes, each deterministic (no atomics):
-//   dK/dV pass: one CTA per 128-key tile, looping over 128-query tiles.
-//   dQ pass:    one CTA per 128-query tile, looping over 128-key tiles.
+// Two forms:
+//   one pass (attn_bwd's): one CTA per 128-key tile, looping over 128-query
+//     tiles, forming dK, dV and every query tile's dQ partial; the partials
+//     are added into a tiled fp32 accumulator by bulk asynchronous reductions
+//     (five MMAs per tile pair; dQ's summation order is not fixed);
+//   two passes, each deterministic (no reductions across CTAs):
+//     dK/dV pass: one CTA per 128-key tile, looping over 128-query tiles;
+//     dQ pass:    one CTA per 128-query tile, looping over 128-key tiles
+//     (seven MMAs per tile pair: dQ's pass recomputes S and dP).
 //
 // Every MMA is M=128 x N=128 x K=16: on this part a tcgen05.mma instruction
 // with N <= 128 costs about the same time whatever N is, so the work is issued
@@ -21,7 +27,9 @@
 //
 // Warps: 0-15 are four compute warpgroups (thread = TMEM lane = row of the
 // CTA's fixed tile); warpgroup x owns columns [32x, 32x+32) of each score
-// tile. Warp 16 is the TMA producer, warp 17 the MMA issuer and TMEM owner.
+// tile. Warp 16 is the TMA producer, warp 17 the MMA issuer and TMEM owner,
+// and in the one-pass kernel warp 18 adds the staged dQ blocks into global
+// memory.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -223,19 +231,8 @@ __device__ __forceinline__ void mma_ss_tile_mnmn(uint32_t d, uint32_t a, uint32_
   }
 }
 
-// Writes 64 bf16 values (32 packed words) as row `r`, column half `half` of a
-// 128 x 128 K-major tile with 128-byte swizzle (the layout TMA produces).
-__device__ __forceinline__ void st_tile_half_row(uint8_t* tile, int r, int half, const uint32_t (&w)[32]) {
-  uint8_t* rowp = tile + half * kColHalf + r * 128;
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
-        make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
-  }
-}
-
 // Writes 32 bf16 values (16 packed words) as columns [32q, 32q+32) of row `r`
-// of a 128 x 128 K-major tile with 128-byte swizzle.
+// of a 128 x 128 K-major tile with 128-byte swizzle (the layout TMA produces).
 __device__ __forceinline__ void st_tile_quarter_row(uint8_t* tile, int r, int q, const uint32_t (&w)[16]) {
   uint8_t* rowp = tile + (q >> 1) * kColHalf + r * 128;
 #pragma unroll

@@ -2,9 +2,11 @@
 // softmax ("EasyContext核心技术解析：序列并行与Flash Attention的完美结合",
 // §2 "Flash Attention优化": tiles of Q, K, V, no stored score matrix).
 //
-// One CTA owns 256 query rows of one (batch, head): two 128-row Q tiles that
-// ping-pong, so the tensor core works on one tile while the softmax warps work
-// on the other.
+// One CTA owns 256 query rows of one (batch, head) in one task: two 128-row Q
+// tiles that ping-pong, so the tensor core works on one tile while the softmax
+// warps work on the other. A launch may carry several tasks (blocks of query
+// rows against blocks of key rows of the same tensors, as the steps of a ring
+// have), laid side by side in one grid; a CTA finds its task by its index.
 //
 //   warp 8      TMA producer: Q tiles once, then K_j, V_j into a 4-slot ring
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM,
