@@ -77,6 +77,49 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(float* __restrict__ o_ac
   }
 }
 
+// Delta for one token row per warp, all heads: the row's H * 256 bytes of O and
+// of dO are read 512 contiguous bytes per instruction (16 bytes a lane, two
+// heads per warp-wide load, four such loads in flight), and each half-warp
+// reduces one head's dot product. Rows must start on 16 bytes and H be even.
+__global__ void __launch_bounds__(256) bwd_preprocess_rows_kernel(const uint4* __restrict__ o,
+                                                                  const uint4* __restrict__ dO, long long rs16,
+                                                                  long long bs16, float* __restrict__ delta,
+                                                                  long long d_hs, long long d_bs, int B, int H, int S) {
+  const long long rows = static_cast<long long>(B) * S;
+  const int ln = threadIdx.x & 31;
+  const int half = ln >> 4;  // which head of the pair this lane's 16 bytes belong to
+  const long long wstep = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows;
+       w += wstep) {
+    const int s = static_cast<int>(w % S);
+    const int b = static_cast<int>(w / S);
+    const long long row = b * bs16 + static_cast<long long>(s) * rs16;
+    for (int h0 = 0; h0 < H; h0 += 8) {
+      float acc[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int hp = h0 + 2 * p;  // heads hp, hp + 1
+        acc[p] = 0.f;
+        if (hp < H) {
+          const uint4 x = __ldg(o + row + hp * (kD / 8) + ln);
+          const uint4 y = __ldg(dO + row + hp * (kD / 8) + ln);
+          const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            acc[p] += bf16lo_to_f32(xs[e]) * bf16lo_to_f32(ys[e]) + bf16hi_to_f32(xs[e]) * bf16hi_to_f32(ys[e]);
+        }
+      }
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+#pragma unroll
+        for (int k = 8; k > 0; k >>= 1) acc[p] += __shfl_xor_sync(0xffffffffu, acc[p], k);
+        const int h = h0 + 2 * p + half;
+        if ((ln & 15) == 0 && h < H) delta[b * d_bs + h * d_hs + s] = acc[p];
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                              const __nv_bfloat16* __restrict__ dO, long long rs,
                                                              long long bs, float* __restrict__ delta, long long d_hs,
@@ -166,6 +209,14 @@ int launch_bwd_preprocess(const void* o, const void* dO, long long row_stride, l
                           long long d_head_stride, long long d_batch_stride, int B, int H, int S, cudaStream_t stream) {
   const long long warps = static_cast<long long>(B) * S * H;
   if (warps == 0) return 0;
+  const bool rows16 = ((reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dO)) & 15u) == 0 &&
+                      row_stride % 8 == 0 && batch_stride % 8 == 0 && H % 2 == 0;
+  if (rows16) {
+    bwd_preprocess_rows_kernel<<<grid_for(static_cast<long long>(B) * S), 256, 0, stream>>>(
+        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), row_stride / 8, batch_stride / 8, delta,
+        d_head_stride, d_batch_stride, B, H, S);
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+  }
   bwd_preprocess_kernel<<<grid_for(warps), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), row_stride, batch_stride, delta,
       d_head_stride, d_batch_stride, B, H, S);
