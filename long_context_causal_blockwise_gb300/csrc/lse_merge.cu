@@ -28,6 +28,71 @@ __device__ __forceinline__ float4 load_bf16x4(const __nv_bfloat16* p) {
   return make_float4(bf16lo_to_f32(u.x), bf16hi_to_f32(u.x), bf16lo_to_f32(u.y), bf16hi_to_f32(u.y));
 }
 
+// The same merge with one warp per token row over all heads, four heads' loads
+// in flight per lane (16 bytes of the fp32 accumulator and 8 or 16 bytes of
+// the block result each). Per element the arithmetic is lse_merge_kernel's.
+__global__ void __launch_bounds__(256) lse_merge_rows_kernel(float* __restrict__ o_acc, float* __restrict__ lse_acc,
+                                                             const void* __restrict__ o_b, int o_b_f32,
+                                                             const float* __restrict__ lse_b, __nv_bfloat16* o_out,
+                                                             int B, int H, int rows, long long o_rs, long long o_bs,
+                                                             long long ob_rs, long long ob_bs, long long l_hs,
+                                                             long long l_bs, long long lb_hs, long long lb_bs) {
+  const long long n = static_cast<long long>(B) * rows;
+  const int ln = threadIdx.x & 31;
+  const long long wstep = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < n; w += wstep) {
+    const int r = static_cast<int>(w % rows);
+    const int b = static_cast<int>(w / rows);
+    for (int h0 = 0; h0 < H; h0 += 4) {
+      float4 oa[4], ob[4];
+      float la[4], lb[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int h = h0 + p;
+        if (h >= H) continue;
+        const long long off = b * o_bs + static_cast<long long>(r) * o_rs + h * kD + ln * 4;
+        const long long boff = b * ob_bs + static_cast<long long>(r) * ob_rs + h * kD + ln * 4;
+        oa[p] = *reinterpret_cast<const float4*>(o_acc + off);
+        ob[p] = o_b_f32 ? __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(o_b) + boff))
+                        : load_bf16x4(static_cast<const __nv_bfloat16*>(o_b) + boff);
+        la[p] = lse_acc[b * l_bs + h * l_hs + r];
+        lb[p] = __ldg(lse_b + b * lb_bs + h * lb_hs + r);
+      }
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int h = h0 + p;
+        if (h >= H) continue;
+        const long long off = b * o_bs + static_cast<long long>(r) * o_rs + h * kD + ln * 4;
+        const float m = fmaxf(la[p], lb[p]);
+        float4 out;
+        float lse;
+        if (m == -INFINITY) {
+          out = make_float4(0.f, 0.f, 0.f, 0.f);
+          lse = -INFINITY;
+        } else {
+          const float wa = __expf(la[p] - m);  // exp(-inf) = 0 for an empty side
+          const float wb = __expf(lb[p] - m);
+          const float den = wa + wb;
+          const float inv = 1.f / den;
+          const float ca = wa * inv, cb = wb * inv;
+          out = make_float4(ca * oa[p].x + cb * ob[p].x, ca * oa[p].y + cb * ob[p].y, ca * oa[p].z + cb * ob[p].z,
+                            ca * oa[p].w + cb * ob[p].w);
+          lse = m + __logf(den);
+        }
+        *reinterpret_cast<float4*>(o_acc + off) = out;
+        if (o_out) {
+          uint2 u;
+          u.x = pack_bf16x2(out.x, out.y);
+          u.y = pack_bf16x2(out.z, out.w);
+          *reinterpret_cast<uint2*>(o_out + off) = u;
+        }
+        __syncwarp();
+        if (ln == 0) lse_acc[b * l_bs + h * l_hs + r] = lse;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) lse_merge_kernel(float* __restrict__ o_acc, float* __restrict__ lse_acc,
                                                         const void* __restrict__ o_b, int o_b_f32,
                                                         const float* __restrict__ lse_b, __nv_bfloat16* o_out,
@@ -197,6 +262,13 @@ int launch_lse_merge(float* o_acc, float* lse_acc, const void* o_b, int o_b_f32,
                      cudaStream_t stream) {
   const long long warps = static_cast<long long>(B) * rows * H;
   if (warps == 0) return 0;
+  if (H >= 4) {
+    lse_merge_rows_kernel<<<grid_for(static_cast<long long>(B) * rows), 256, 0, stream>>>(
+        o_acc, lse_acc, o_b, o_b_f32, lse_b, static_cast<__nv_bfloat16*>(o_out_bf16), B, H, rows, o_row_stride,
+        o_batch_stride, ob_row_stride, ob_batch_stride, lse_head_stride, lse_batch_stride, lseb_head_stride,
+        lseb_batch_stride);
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+  }
   lse_merge_kernel<<<grid_for(warps), 256, 0, stream>>>(o_acc, lse_acc, o_b, o_b_f32, lse_b,
                                                         static_cast<__nv_bfloat16*>(o_out_bf16), B, H, rows,
                                                         o_row_stride, o_batch_stride, ob_row_stride,

@@ -134,8 +134,11 @@ def test_lse_merge_matches_oracle_and_split_equals_monolithic():
     assert_lse_close(to64(lse_acc), L)
 
 
-def test_lse_merge_empty_sides():
-    B, H, R = 1, 2, 64
+@pytest.mark.parametrize("B,H", [(1, 2), (2, 6)])
+def test_lse_merge_empty_sides(B, H):
+    """Both merge kernels (a warp per (row, head) for H < 4, a warp per row over
+    the heads otherwise, here with a partial group of heads)."""
+    R = 64
     o_acc = torch.randn(B, R, H, D, device="cuda")
     lse_acc = torch.randn(B, H, R, device="cuda")
     lse_acc[:, :, ::3] = -math.inf
@@ -153,8 +156,10 @@ def test_lse_merge_empty_sides():
     np.testing.assert_allclose(got_l[fin], want[1][fin], atol=1e-5)
 
 
-def test_preprocess_delta():
-    B, H, S = 2, 3, 777
+@pytest.mark.parametrize("H", [3, 4, 10])
+def test_preprocess_delta(H):
+    """Both preprocess kernels (odd H: a warp per (row, head); even H: a warp per row)."""
+    B, S = 2, 777
     o, do, _, _ = gaussian_qkvdo(B, H, S, D, seed=9, with_do=False)
     delta = torch.empty(B, H, S, device="cuda")
     lcb.attn_bwd_preprocess(o, do, delta)
