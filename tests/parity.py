@@ -36,6 +36,20 @@ def assert_bf16_close(got, want, name, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
     return mx, mean, rel
 
 
+def assert_bf16_close_scaled(got, want, name, max_rel=MAX_ABS, mean_abs=MEAN_ABS):
+    """The bf16 bars with the maximum taken relative to max(1, |want|): for
+    outputs larger than 1 in magnitude half a bf16 step alone reaches the
+    absolute bar (0.0156 at 4, 0.031 at 8), so there the bar is relative."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    scaled = np.abs(got - want) / np.maximum(1.0, np.abs(want))
+    mx, mean, rel = err_stats(got, want)
+    assert scaled.max() <= max_rel and mean <= mean_abs, (
+        f"{name}: scaled max {scaled.max():.3e} (bar {max_rel}), max-abs {mx:.3e}, mean-abs {mean:.3e} "
+        f"(bar {mean_abs}), rel-L2 {rel:.3e}")
+
+
 def assert_lse_close(got, want, name="lse", tol=LSE_ABS):
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)

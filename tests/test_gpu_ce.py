@@ -100,3 +100,13 @@ def test_ce_llama_vocab_32768_tokens_sampled():
     torch.cuda.synchronize()
     _check(x_rows, y[rows_d], loss[rows_d], lse[rows_d], x[rows_d])
     assert torch.isfinite(x).all()
+
+
+def test_ce_largest_staged_vocabulary():
+    """V = 100000 (a 200 KB row, one CTA per SM), fused forward and backward."""
+    N, V = 48, 100000
+    x, y = _case(N, V, seed=17, ignore_frac=0.0)
+    x0 = x.clone()
+    loss, lse = lcb.cross_entropy(x, y, mode="fwd_bwd")
+    torch.cuda.synchronize()
+    _check(x0, y, loss, lse, x)

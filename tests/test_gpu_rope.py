@@ -24,7 +24,7 @@ def _rope_err(got, want, x):
     return np.abs(got - want) / bound
 
 
-@pytest.mark.parametrize("theta,pos0", [(1e4, 0), (1e6, 0), (1e6, 500_000), (1e9, 1_000_000)])
+@pytest.mark.parametrize("theta,pos0", [(1e4, 0), (1e6, 0), (1e6, 500_000), (1e9, 1_000_000), (1e6, 1_000_000_000)])
 def test_rope_matches_oracle(theta, pos0):
     """Every element within one bf16 step of the fp64 rotation rounded to bf16,
     almost all of them equal; the inverse undoes it within bf16 rounding."""
