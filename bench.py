@@ -546,12 +546,16 @@ def run_rope(args):
 def run_ce(args):
     """Times the cross-entropy loss head, forward and in-place backward in one
     pass, on Llama-2's vocabulary (V = 32000) over a 32768-token sequence
-    (2.1 GB of bf16 logits); prints one JSON line (not the headline bench line)."""
+    (2.1 GB of bf16 logits), or with --vocab V over as many tokens as keep the
+    logits near that size (V = 128256, Llama-3: 8192 tokens, rows streamed);
+    prints one JSON line (not the headline bench line). Bytes are the
+    algorithmic ones: logits read once (and written once with the backward)."""
     import torch
 
     import long_context_causal_blockwise_gb300 as lcb
 
-    N, V = 32768, 32000
+    V = args.vocab
+    N = max(1, 32768 * 32000 // V)
     dev = torch.device("cuda", 0)
     lcb.load()
     g = torch.Generator(device=dev).manual_seed(0)
@@ -579,7 +583,7 @@ def run_ce(args):
     nb_fb = 2 * N * V * 2 + N * (8 + 8)
     _, _, hbm, src = load_peaks()
     print(json.dumps({
-        "metric": "cross-entropy loss head, V=32000, N=32768 tokens, bf16 logits",
+        "metric": f"cross-entropy loss head, V={V}, N={N} tokens, bf16 logits",
         "fwd_bwd_ms": t_fb, "fwd_ms": t_fwd, "tokens_per_s_fwd_bwd": N / t_fb * 1e3,
         "fwd_bwd_gbs": nb_fb / t_fb / 1e6, "fwd_gbs": nb_fwd / t_fwd / 1e6,
         "fwd_bwd_frac_of_hbm": nb_fb / t_fb / 1e6 / hbm, "fwd_frac_of_hbm": nb_fwd / t_fwd / 1e6 / hbm,
@@ -597,6 +601,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--H", type=int, default=H, help="heads (profiling of smaller cases only)")
     ap.add_argument("--S", type=int, default=S, help="sequence length (profiling of smaller cases only)")
+    ap.add_argument("--vocab", type=int, default=32000, help="vocabulary size of --ce")
     ap.add_argument("--ce", action="store_true",
                     help="time the cross-entropy loss head (V=32000, 32768 tokens)")
     ap.add_argument("--rope", action="store_true",

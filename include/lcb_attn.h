@@ -324,9 +324,10 @@ int zigzag_schedule(int S, int P, int* perm, lcb_task* tasks);
  *   x_ij   <- dloss[i] * (exp(x_ij - lse[i]) - [j == y_i])   (bf16, in place)
  * dloss: fp32 [N] DEVICE, NULL meaning 1 for every row. A row whose label is
  * ignore_index gets loss 0 and a zero gradient; a label outside [0, V)
- * otherwise gives loss NaN (and no one-hot term). Each row is staged whole in
- * shared memory: V * 2 bytes must fit next to a few hundred bytes of
- * bookkeeping in 227 KB (V <= 115000), else LCB_ERR_UNSUPPORTED.
+ * otherwise gives loss NaN (and no one-hot term). Any V >= 1: rows are
+ * streamed through registers, many in flight per SM; with LCB_CE_FWD_BWD the
+ * gradient pass reads each row a second time, from L2 (HBM: one read, and
+ * one write with the gradient).
  */
 int lcb_cross_entropy(void* logits, const long long* labels, float* loss, float* lse, const float* dloss, int N,
                       int V, long long row_stride, int ignore_index, int mode, void* stream);

@@ -648,13 +648,8 @@ int lcb_cross_entropy(void* logits, const long long* labels, float* loss, float*
   if (mode != LCB_CE_FWD && mode != LCB_CE_FWD_BWD && mode != LCB_CE_BWD) return LCB_ERR_UNSUPPORTED;
   if (N == 0) return LCB_OK;
   if (!logits || !labels || !lse || (reinterpret_cast<uintptr_t>(logits) & 1u)) return LCB_ERR_ARG;
-  if (static_cast<size_t>(V) * 2 + 1024 > 232448) return LCB_ERR_UNSUPPORTED;
-  DevStatus ds;
-  int rc = dev_status(&ds);
-  if (rc != LCB_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return finish(launch_cross_entropy(logits, labels, loss, lse, dloss, N, V, row_stride, ignore_index, mode, ds, st),
-                st);
+  return finish(launch_cross_entropy(logits, labels, loss, lse, dloss, N, V, row_stride, ignore_index, mode, st), st);
 }
 
 int lcb_rope(const void* x, void* y, int B, int S, int H, int D, double theta, long long pos0, int inverse,

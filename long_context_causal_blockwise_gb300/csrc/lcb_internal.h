@@ -97,9 +97,9 @@ int launch_wait_selftest(DevStatus st, cudaStream_t stream);
 
 int launch_cast_f32_bf16(const float* src, void* dst, long long n, cudaStream_t stream);
 
-// Cross-entropy over rows of bf16 logits staged in shared memory (mode LCB_CE_*).
+// Cross-entropy over rows of bf16 logits streamed through registers (mode LCB_CE_*).
 int launch_cross_entropy(void* logits, const long long* labels, float* loss, float* lse, const float* dloss, int N,
-                         int V, long long row_stride, int ignore_index, int mode, DevStatus st, cudaStream_t stream);
+                         int V, long long row_stride, int ignore_index, int mode, cudaStream_t stream);
 
 // RoPE frequencies f_k = theta^(-2k/128), k < 64, computed on the host in fp64.
 struct RopeFreqs {

@@ -41,10 +41,14 @@ def _check(x0, y, loss, lse, grad, rows=None, dloss=None):
         assert err.max() <= 1.0, err.max()
 
 
-@pytest.mark.parametrize("N,V", [(100, 1000), (37, 1001), (5, 8), (3, 1)])
+@pytest.mark.parametrize("N,V", [(100, 1000), (37, 1001), (5, 8), (3, 1), (5000, 1000), (400, 57344), (40, 128256),
+                                 (9, 120001), (1, 128256)])
 def test_ce_modes_vs_oracle(N, V):
-    """fwd, fwd_bwd (in place) and bwd from a saved LSE; aligned rows go through
-    bulk copies, V = 1001 and 1 through plain loads."""
+    """fwd, fwd_bwd (in place) and bwd from a saved LSE. Aligned rows that fit
+    in shared memory go through bulk copies (N = 5000: each CTA's ring of three
+    row slots wraps a few times; V = 57344: two slots), V = 1001 and 1 through
+    plain loads; V = 128256 (Llama-3) and 120001 are longer than shared memory
+    and are streamed from global memory (16-byte and scalar loads)."""
     x, y = _case(N, V, seed=N + V)
     x0 = x.clone()
     loss, lse = lcb.cross_entropy(x, y, mode="fwd")
@@ -102,8 +106,9 @@ def test_ce_llama_vocab_32768_tokens_sampled():
     assert torch.isfinite(x).all()
 
 
-def test_ce_largest_staged_vocabulary():
-    """V = 100000 (a 200 KB row, one CTA per SM), fused forward and backward."""
+def test_ce_wide_vocabulary_all_rows():
+    """V = 100000 (200 KB rows, the 1024-thread launch shape), fused forward
+    and backward, every row checked."""
     N, V = 48, 100000
     x, y = _case(N, V, seed=17, ignore_frac=0.0)
     x0 = x.clone()
