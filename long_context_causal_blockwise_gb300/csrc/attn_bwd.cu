@@ -574,7 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // staging slots for dQ blocks (warpgroups x and x + 2 share slot x & 1).
 // Warps 0-15 compute, 16 TMA producer, 17 MMA issuer, 18 dQ reducer.
 // MMA order per query tile i: dV += P^T dO_i, S^T(i+1), dQ(i),
-// dK += dS^T Q_i, then dP^T(i+1) once dQ(i) has been read out.
+// dK += dS^T Q_i, then dP^T(i+1) once dQ(i) has been read out. The compute
+// warps form dS^T(i), then P^T(i+1) while dQ(i) and dK(i) run, then read
+// out and stage dQ(i).
 constexpr int kFuThreads = 608;
 constexpr int kFuReduceWarp = 18;
 constexpr uint32_t kDqBlock = 128 * 32 * 4;  // one staged dQ block: 128 rows x 32 columns fp32
@@ -787,86 +789,101 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     float nl2 = 0.f, ndl = 0.f;
     if (n > 0) load_stats(0, nl2, ndl);
     bool ok = true;
-    for (int i = 0; i < n && ok; ++i) {
-      const uint32_t ph = static_cast<uint32_t>(i) & 1u;
-      const int it = i0 + i;            // query tile
-      const int qx = it * kT + 32 * x;  // first query of this warpgroup's columns
-      const float l2v = nl2, dlv = ndl;
-      if (i + 1 < n) load_stats(i + 1, nl2, ndl);
-      ok = warp_all(mbar_wait(&bars->s_full, ph, abort_flag, p.st, kWhere | (5u << 16)));
-      if (!ok) break;
-      tc_fence_after();
-      const bool diag = causal && (it == kt);
-      // Phase 1: P^T, into this warpgroup's own S^T columns (already read by it).
-      float pv[32];
-      {
-        uint32_t s[32];
-        tmem_ld_x32(tS + lane_off + 32 * x, s);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float l2 = __shfl_sync(0xffffffffu, l2v, e);
-          float pe = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2));
-          if ((diag && qx + e < j) || !key_ok) pe = 0.f;
-          pv[e] = pe;
-        }
-      }
-      {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(pv[e], pv[e + 1]);
-        tmem_st_x16_nowait(tS + lane_off + 32 * x, pk);
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->pt_full);  // dV(i) and S^T(i+1) may go
-      // Phase 2: dS^T = P^T (dP^T - Delta), into shared memory for dK and dQ.
-      ok = warp_all(mbar_wait(&bars->dp_full, ph, abort_flag, p.st, kWhere | (6u << 16)));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t dk[16];
-      {
-        uint32_t dp[32];
-        tmem_ld_x32(tDP + lane_off + 32 * x, dp);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float d0 = __shfl_sync(0xffffffffu, dlv, e);
-          const float d1 = __shfl_sync(0xffffffffu, dlv, e + 1);
-          dk[e >> 1] =
-              pack_bf16x2(pv[e] * (__uint_as_float(dp[e]) - d0), pv[e + 1] * (__uint_as_float(dp[e + 1]) - d1));
-        }
-      }
-      if (i > 0) {
-        ok = warp_all(mbar_wait(&bars->ds_free, ph ^ 1u, abort_flag, p.st, kWhere | (9u << 16)));
+    // Step s runs phase 2 of query tile s-1, phase 1 of tile s, then phase 3
+    // of tile s-1: P^T(s) is computed while the tensor pipe runs dQ(s-1) and
+    // dK(s-1), so the next dV and S^T can be issued as soon as dP^T(s) is.
+    float pv[32];      // P^T of the tile between its phases 1 and 2
+    float dl2 = 0.f;   // Delta of that tile
+    for (int s = 0; s <= n && ok; ++s) {
+      if (s > 0) {
+        // Phase 2: dS^T = P^T (dP^T - Delta), into shared memory for dK and dQ.
+        const int i = s - 1;
+        const uint32_t ph = static_cast<uint32_t>(i) & 1u;
+        ok = warp_all(mbar_wait(&bars->dp_full, ph, abort_flag, p.st, kWhere | (6u << 16)));
         if (!ok) break;
-      }
-      st_tile_quarter_row(ds_tile, row, x, dk);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full);  // also: dP^T(i) is in registers, its columns may take dQ(i)
-      // Phase 3: row `row` of dQ(i) (TMEM lane = query row), columns [32x, 32x + 32), staged for the reducer.
-      ok = warp_all(mbar_wait(&bars->dq_full, ph, abort_flag, p.st, kWhere | (7u << 16)));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t g[32];
-      tmem_ld_x32(tDQ + lane_off + 32 * x, g);
-      tc_fence_before();
-      mbar_arrive(&bars->dq_free);
-      // slot x & 1 is free once the other warpgroup's block in it was read:
-      // warpgroups 0/1 wait for 2/3's block of tile i-1, 2/3 for 0/1's block of tile i.
-      if (x < 2) {
-        if (i > 0) ok = warp_all(mbar_wait(&bars->stg_free[x + 2], ph ^ 1u, abort_flag, p.st, kWhere | (15u << 16)));
-      } else {
-        ok = warp_all(mbar_wait(&bars->stg_free[x - 2], ph, abort_flag, p.st, kWhere | (15u << 16)));
-      }
-      if (!ok) break;
+        tc_fence_after();
+        uint32_t dk[16];
+        {
+          uint32_t dp[32];
+          tmem_ld_x32(tDP + lane_off + 32 * x, dp);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        *reinterpret_cast<float4*>(stg_row + ((ch ^ (row & 7)) << 4)) =
-            make_float4(__uint_as_float(g[4 * ch]) * p.scale, __uint_as_float(g[4 * ch + 1]) * p.scale,
-                        __uint_as_float(g[4 * ch + 2]) * p.scale, __uint_as_float(g[4 * ch + 3]) * p.scale);
+          for (int e = 0; e < 32; e += 2) {
+            const float d0 = __shfl_sync(0xffffffffu, dl2, e);
+            const float d1 = __shfl_sync(0xffffffffu, dl2, e + 1);
+            dk[e >> 1] =
+                pack_bf16x2(pv[e] * (__uint_as_float(dp[e]) - d0), pv[e + 1] * (__uint_as_float(dp[e + 1]) - d1));
+          }
+        }
+        if (i > 0) {
+          ok = warp_all(mbar_wait(&bars->ds_free, ph ^ 1u, abort_flag, p.st, kWhere | (9u << 16)));
+          if (!ok) break;
+        }
+        st_tile_quarter_row(ds_tile, row, x, dk);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full);  // also: dP^T(i) is in registers, its columns may take dQ(i)
       }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->stg_full[x]);
+      if (s < n) {
+        // Phase 1: P^T(s), into this warpgroup's own S^T columns (already read by it).
+        const int it = i0 + s;            // query tile
+        const int qx = it * kT + 32 * x;  // first query of this warpgroup's columns
+        const float l2v = nl2;
+        dl2 = ndl;
+        if (s + 1 < n) load_stats(s + 1, nl2, ndl);
+        ok = warp_all(mbar_wait(&bars->s_full, static_cast<uint32_t>(s) & 1u, abort_flag, p.st, kWhere | (5u << 16)));
+        if (!ok) break;
+        tc_fence_after();
+        const bool diag = causal && (it == kt);
+        {
+          uint32_t sv[32];
+          tmem_ld_x32(tS + lane_off + 32 * x, sv);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float l2 = __shfl_sync(0xffffffffu, l2v, e);
+            float pe = ex2_approx(fmaf(__uint_as_float(sv[e]), c, -l2));
+            if ((diag && qx + e < j) || !key_ok) pe = 0.f;
+            pv[e] = pe;
+          }
+        }
+        {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(pv[e], pv[e + 1]);
+          tmem_st_x16_nowait(tS + lane_off + 32 * x, pk);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->pt_full);  // dV(s) and S^T(s+1) may go
+      }
+      if (s > 0) {
+        // Phase 3: row `row` of dQ(i) (TMEM lane = query row), columns [32x, 32x + 32), staged for the reducer.
+        const int i = s - 1;
+        const uint32_t ph = static_cast<uint32_t>(i) & 1u;
+        ok = warp_all(mbar_wait(&bars->dq_full, ph, abort_flag, p.st, kWhere | (7u << 16)));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t g[32];
+        tmem_ld_x32(tDQ + lane_off + 32 * x, g);
+        tc_fence_before();
+        mbar_arrive(&bars->dq_free);
+        // slot x & 1 is free once the other warpgroup's block in it was read:
+        // warpgroups 0/1 wait for 2/3's block of tile i-1, 2/3 for 0/1's block of tile i.
+        if (x < 2) {
+          if (i > 0)
+            ok = warp_all(mbar_wait(&bars->stg_free[x + 2], ph ^ 1u, abort_flag, p.st, kWhere | (15u << 16)));
+        } else {
+          ok = warp_all(mbar_wait(&bars->stg_free[x - 2], ph, abort_flag, p.st, kWhere | (15u << 16)));
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          *reinterpret_cast<float4*>(stg_row + ((ch ^ (row & 7)) << 4)) =
+              make_float4(__uint_as_float(g[4 * ch]) * p.scale, __uint_as_float(g[4 * ch + 1]) * p.scale,
+                          __uint_as_float(g[4 * ch + 2]) * p.scale, __uint_as_float(g[4 * ch + 3]) * p.scale);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->stg_full[x]);
+      }
     }
     // Epilogue: warpgroups 0/1 write dV columns [0,64)/[64,128), 2/3 write dK (scaled).
     const bool valid = j < Sk;
