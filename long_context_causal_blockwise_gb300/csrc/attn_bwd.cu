@@ -750,20 +750,28 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     }
     __syncwarp();
   } else if (warp == kFuReduceWarp) {
-    // Adds each staged 16 KB dQ block into the accumulator; frees its slot once read.
+    // Adds each staged 16 KB dQ block into the accumulator; frees its slot once
+    // read. Blocks x and x + 1 sit in different slots, so both reductions are
+    // issued before the first read is waited for: the two reads overlap.
     if (lane == 0 && n > 0) {
       bool ok = true;
       for (int i = 0; i < n && ok; ++i) {
         const uint32_t ph = static_cast<uint32_t>(i) & 1u;
         float* tile =
             p.dq_acc + b * p.dq_bs + h * p.dq_hs + static_cast<long long>(q_off / kT + i0 + i) * (kT * kD);
-        for (int x = 0; x < 4 && ok; ++x) {  // blocks 0, 1, then 2, 3 reusing the slots
+        for (int x = 0; x < 4 && ok; x += 2) {  // blocks 0, 1 in slots 0, 1, then 2, 3 reusing them
           ok = mbar_wait(&bars->stg_full[x], ph, abort_flag, p.st, kWhere | (14u << 16));
           if (!ok) break;
-          bulk_reduce_add_f32(tile + x * (kDqBlock / 4), sbase + kFuSmStg + (x & 1) * kDqBlock, kDqBlock);
+          bulk_reduce_add_f32(tile + x * (kDqBlock / 4), sbase + kFuSmStg, kDqBlock);
           bulk_commit();
-          bulk_wait_read<0>();
+          ok = mbar_wait(&bars->stg_full[x + 1], ph, abort_flag, p.st, kWhere | (14u << 16));
+          if (!ok) break;
+          bulk_reduce_add_f32(tile + (x + 1) * (kDqBlock / 4), sbase + kFuSmStg + kDqBlock, kDqBlock);
+          bulk_commit();
+          bulk_wait_read<1>();  // block x has left its slot
           mbar_arrive(&bars->stg_free[x]);
+          bulk_wait_read<0>();
+          mbar_arrive(&bars->stg_free[x + 1]);
         }
       }
       bulk_wait_all();  // every reduction issued has completed
