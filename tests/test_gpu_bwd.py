@@ -290,3 +290,21 @@ def test_batch_of_four_full_tensors():
     assert_lse_close(to64(lse), ref["lse"])
     for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
         assert_bf16_close_scaled(to64(got), ref[name], f"{name} B4")
+
+
+@pytest.mark.parametrize("B,H,S", [(2, 3, 300), (1, 32, 4096), (1, 1, 1)])
+def test_dq_untile_both_store_widths(B, H, S):
+    """lcb_dq_untile is a layout change plus one bf16 rounding: bit-exact
+    against undoing the documented tile layout in torch, through the 16-byte
+    store path (aligned contiguous rows) and the 8-byte path (a row stride of
+    H*128 + 4 elements); the padding of the strided rows is not touched."""
+    g = torch.Generator(device="cuda").manual_seed(B * 1000 + H * 10 + S)
+    tiles = torch.randn(B, H, (S + 127) // 128, 128 * 128, generator=g, device="cuda") * 3
+    want = untile_f32(tiles, S).to(torch.bfloat16)
+    dq = lcb.dq_untile(tiles, torch.empty(B, S, H, D, dtype=torch.bfloat16, device="cuda"))
+    buf = torch.full((B, S, H * D + 4), 7.0, dtype=torch.bfloat16, device="cuda")
+    dq_s = lcb.dq_untile(tiles, buf.as_strided((B, S, H, D), (S * (H * D + 4), H * D + 4, D, 1)))
+    torch.cuda.synchronize()
+    assert torch.equal(dq, want)
+    assert torch.equal(dq_s, want)
+    assert (buf[:, :, H * D:] == 7.0).all()
