@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "lcb_internal.h"
 
@@ -28,41 +29,56 @@ __device__ __forceinline__ float4 load_bf16x4(const __nv_bfloat16* p) {
   return make_float4(bf16lo_to_f32(u.x), bf16hi_to_f32(u.x), bf16lo_to_f32(u.y), bf16hi_to_f32(u.y));
 }
 
-// The same merge with one warp per token row over all heads, four heads' loads
-// in flight per lane (16 bytes of the fp32 accumulator and 8 or 16 bytes of
-// the block result each). Per element the arithmetic is lse_merge_kernel's.
-__global__ void __launch_bounds__(256) lse_merge_rows_kernel(float* __restrict__ o_acc, float* __restrict__ lse_acc,
-                                                             const void* __restrict__ o_b, int o_b_f32,
-                                                             const float* __restrict__ lse_b, __nv_bfloat16* o_out,
-                                                             int B, int H, int rows, long long o_rs, long long o_bs,
-                                                             long long ob_rs, long long ob_bs, long long l_hs,
-                                                             long long l_bs, long long lb_hs, long long lb_bs) {
+// The same merge with one warp per token row over all heads, eight heads'
+// loads in flight per lane (16 bytes of the fp32 accumulator and 8 or 16
+// bytes of the block result each); the row's base addresses are formed once,
+// the block's dtype and the bf16 copy out are template parameters. Per element
+// the arithmetic is lse_merge_kernel's.
+template <bool kObF32, bool kOut>
+__global__ void __launch_bounds__(256, 2) lse_merge_rows_kernel(float* __restrict__ o_acc, float* __restrict__ lse_acc,
+                                                                const void* __restrict__ o_b,
+                                                                const float* __restrict__ lse_b, __nv_bfloat16* o_out,
+                                                                int B, int H, int rows, long long o_rs, long long o_bs,
+                                                                long long ob_rs, long long ob_bs, long long l_hs,
+                                                                long long l_bs, long long lb_hs, long long lb_bs) {
+  constexpr int G = 8;
+  using BT = typename std::conditional<kObF32, float, __nv_bfloat16>::type;
   const long long n = static_cast<long long>(B) * rows;
   const int ln = threadIdx.x & 31;
   const long long wstep = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < n; w += wstep) {
     const int r = static_cast<int>(w % rows);
     const int b = static_cast<int>(w / rows);
-    for (int h0 = 0; h0 < H; h0 += 4) {
-      float4 oa[4], ob[4];
-      float la[4], lb[4];
+    // per-row bases, advanced by one group of heads per iteration: the heads
+    // of a group sit at fixed offsets (p * 128 values) from them
+    float* pa = o_acc + b * o_bs + static_cast<long long>(r) * o_rs + ln * 4;
+    const BT* pb = static_cast<const BT*>(o_b) + b * ob_bs + static_cast<long long>(r) * ob_rs + ln * 4;
+    __nv_bfloat16* po = kOut ? o_out + b * o_bs + static_cast<long long>(r) * o_rs + ln * 4 : nullptr;
+    float* pla = lse_acc + b * l_bs + r;
+    const float* plb = lse_b + b * lb_bs + r;
+    for (int h0 = 0; h0 < H; h0 += G, pa += G * kD, pb += G * kD, po += kOut ? G * kD : 0) {
+      float4 oa[G], ob[G];
+      float la[G], lb[G];
+      {
+        const float* qa = pla;
+        const float* qb = plb;
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int h = h0 + p;
-        if (h >= H) continue;
-        const long long off = b * o_bs + static_cast<long long>(r) * o_rs + h * kD + ln * 4;
-        const long long boff = b * ob_bs + static_cast<long long>(r) * ob_rs + h * kD + ln * 4;
-        oa[p] = *reinterpret_cast<const float4*>(o_acc + off);
-        ob[p] = o_b_f32 ? __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(o_b) + boff))
-                        : load_bf16x4(static_cast<const __nv_bfloat16*>(o_b) + boff);
-        la[p] = lse_acc[b * l_bs + h * l_hs + r];
-        lb[p] = __ldg(lse_b + b * lb_bs + h * lb_hs + r);
+        for (int p = 0; p < G; ++p, qa += l_hs, qb += lb_hs) {
+          if (h0 + p >= H) continue;
+          oa[p] = *reinterpret_cast<const float4*>(pa + p * kD);
+          if constexpr (kObF32) {
+            ob[p] = __ldg(reinterpret_cast<const float4*>(pb + p * kD));
+          } else {
+            ob[p] = load_bf16x4(pb + p * kD);
+          }
+          la[p] = *qa;
+          lb[p] = __ldg(qb);
+        }
       }
+      __syncwarp();  // every lane has read the group's LSE before lane 0 overwrites it
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int h = h0 + p;
-        if (h >= H) continue;
-        const long long off = b * o_bs + static_cast<long long>(r) * o_rs + h * kD + ln * 4;
+      for (int p = 0; p < G; ++p, pla += l_hs, plb += lb_hs) {
+        if (h0 + p >= H) continue;
         const float m = fmaxf(la[p], lb[p]);
         float4 out;
         float lse;
@@ -79,15 +95,14 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(float* __restrict__
                             ca * oa[p].w + cb * ob[p].w);
           lse = m + __logf(den);
         }
-        *reinterpret_cast<float4*>(o_acc + off) = out;
-        if (o_out) {
+        *reinterpret_cast<float4*>(pa + p * kD) = out;
+        if constexpr (kOut) {
           uint2 u;
           u.x = pack_bf16x2(out.x, out.y);
           u.y = pack_bf16x2(out.z, out.w);
-          *reinterpret_cast<uint2*>(o_out + off) = u;
+          *reinterpret_cast<uint2*>(po + p * kD) = u;
         }
-        __syncwarp();
-        if (ln == 0) lse_acc[b * l_bs + h * l_hs + r] = lse;
+        if (ln == 0) *pla = lse;
       }
     }
   }
@@ -263,10 +278,15 @@ int launch_lse_merge(float* o_acc, float* lse_acc, const void* o_b, int o_b_f32,
   const long long warps = static_cast<long long>(B) * rows * H;
   if (warps == 0) return 0;
   if (H >= 4) {
-    lse_merge_rows_kernel<<<grid_for(static_cast<long long>(B) * rows), 256, 0, stream>>>(
-        o_acc, lse_acc, o_b, o_b_f32, lse_b, static_cast<__nv_bfloat16*>(o_out_bf16), B, H, rows, o_row_stride,
-        o_batch_stride, ob_row_stride, ob_batch_stride, lse_head_stride, lse_batch_stride, lseb_head_stride,
-        lseb_batch_stride);
+    // a warp per token row (two CTAs of 8 warps resident per SM at 128
+    // registers a thread), eight heads' loads of every warp in flight
+    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>((static_cast<long long>(B) * rows + 7) / 8, kSMs * 8LL)));
+    auto* out = static_cast<__nv_bfloat16*>(o_out_bf16);
+    auto kernel = o_b_f32 ? (out ? lse_merge_rows_kernel<true, true> : lse_merge_rows_kernel<true, false>)
+                          : (out ? lse_merge_rows_kernel<false, true> : lse_merge_rows_kernel<false, false>);
+    kernel<<<grid, 256, 0, stream>>>(o_acc, lse_acc, o_b, lse_b, out, B, H, rows, o_row_stride, o_batch_stride,
+                                     ob_row_stride, ob_batch_stride, lse_head_stride, lse_batch_stride,
+                                     lseb_head_stride, lseb_batch_stride);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
   }
   lse_merge_kernel<<<grid_for(warps), 256, 0, stream>>>(o_acc, lse_acc, o_b, o_b_f32, lse_b,

@@ -156,6 +156,34 @@ def test_lse_merge_empty_sides(B, H):
     np.testing.assert_allclose(got_l[fin], want[1][fin], atol=1e-5)
 
 
+@pytest.mark.parametrize("ob_f32,with_out", [(False, False), (False, True), (True, False), (True, True)])
+def test_lse_merge_rows_kernel_all_forms(ob_f32, with_out):
+    """The row kernel's four forms (block result bf16 or fp32, with or without
+    the bf16 copy out), B = 2 and H = 12 (a group of eight heads and a partial
+    one), against the oracle; the copy out is the merged fp32 value rounded
+    once."""
+    B, H, R = 2, 12, 200
+    g = torch.Generator(device="cuda").manual_seed(5 + 2 * ob_f32 + with_out)
+    o_acc = torch.randn(B, R, H, D, generator=g, device="cuda")
+    lse_acc = torch.randn(B, H, R, generator=g, device="cuda") * 4
+    lse_acc[:, :, ::5] = -math.inf
+    o_b = torch.randn(B, R, H, D, generator=g, device="cuda")
+    o_b = o_b if ob_f32 else o_b.to(torch.bfloat16)
+    lse_b = torch.randn(B, H, R, generator=g, device="cuda") * 4
+    lse_b[:, :, ::7] = -math.inf
+    want = oracle.lse_merge(to64(o_acc), to64(lse_acc), to64(o_b), to64(lse_b))
+    o_out = torch.empty(B, R, H, D, dtype=torch.bfloat16, device="cuda") if with_out else None
+    lcb.attn_lse_merge(o_acc, lse_acc, o_b, lse_b, o_out_bf16=o_out)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(to64(o_acc), want[0], atol=1e-5)
+    got_l = to64(lse_acc)
+    assert np.array_equal(np.isneginf(got_l), np.isneginf(want[1]))
+    fin = np.isfinite(want[1])
+    np.testing.assert_allclose(got_l[fin], want[1][fin], atol=1e-5)
+    if with_out:
+        assert torch.equal(o_out, o_acc.to(torch.bfloat16))
+
+
 @pytest.mark.parametrize("H", [3, 4, 10])
 def test_preprocess_delta(H):
     """Both preprocess kernels (odd H: a warp per (row, head); even H: a warp per row)."""
