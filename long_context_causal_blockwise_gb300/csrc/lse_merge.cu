@@ -280,7 +280,8 @@ int launch_lse_merge(float* o_acc, float* lse_acc, const void* o_b, int o_b_f32,
   if (H >= 4) {
     // a warp per token row (two CTAs of 8 warps resident per SM at 128
     // registers a thread), eight heads' loads of every warp in flight
-    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>((static_cast<long long>(B) * rows + 7) / 8, kSMs * 8LL)));
+    const long long row_warps = static_cast<long long>(B) * rows;
+    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>((row_warps + 7) / 8, kSMs * 8LL)));
     auto* out = static_cast<__nv_bfloat16*>(o_out_bf16);
     auto kernel = o_b_f32 ? (out ? lse_merge_rows_kernel<true, true> : lse_merge_rows_kernel<true, false>)
                           : (out ? lse_merge_rows_kernel<false, true> : lse_merge_rows_kernel<false, false>);
