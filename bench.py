@@ -72,6 +72,12 @@ def fwd_flop(b, h, s, d):
     return 2.0 * b * h * s * s * d
 
 
+def input_checksums(named):
+    """fp64 sum of the first 2^20 elements of each generated input (outside any
+    timed region), so that a record identifies the synthetic data it ran on."""
+    return {n: float(t.reshape(-1)[: 1 << 20].double().sum()) for n, t in named}
+
+
 def kernel_source_hash(files):
     """sha256 over the kernel sources a recorded ncu figure was taken from."""
     import hashlib
@@ -220,7 +226,9 @@ def run_reference(args, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B, "H": H, "S": S, "D": D, "causal": True,
                    "global_batch": 1, "seq_len": S, "parallelism": "host cores"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                         "extrapolated_full_step_s": step_flop(B, H, S, D) / (value * 1e12),
+                         "extrapolated_note": "extrapolated: the full step's FLOPs at the sample's rate"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -239,6 +247,7 @@ def run_ours(args, rank, world, local_rank):
     lcb.load()
     scale = D ** -0.5
     q, k, v, do = gaussian_qkvdo(B, H, S, D, seed=rank, device=dev)
+    checksums = input_checksums((("q", q), ("k", k), ("v", v), ("do", do)))
     o = torch.empty_like(q)
     lse = torch.empty(B, H, S, device=dev)
     delta = torch.empty(B, H, S, device=dev)
@@ -399,7 +408,8 @@ def run_ours(args, rank, world, local_rank):
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B, "H": H, "S": S, "D": D, "causal": True, "l2": L2_NOTE,
-                   "global_batch": world, "seq_len": S, "parallelism": f"dp{world} (one independent layer per GPU)"},
+                   "global_batch": world, "seq_len": S, "parallelism": f"dp{world} (one independent layer per GPU)",
+                   "input_checksum_f64": checksums},
         "pct_of_peak": 100.0 * (value / world) / sus,
         "peak_tflops": sus, "peak_source": f"{src} bf16 sustained",
         "fwd_tflops": fwd_flop(B, H, S, D) / fwd_t / 1e12,
@@ -420,7 +430,9 @@ def run_ours(args, rank, world, local_rank):
         dt, cflop = cpu_oracle_sample(q, k, v, do, CPU_SAMPLE_S)
         line["cpu_baseline"] = {
             "value": cflop / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd of head 0's causal prefix of {CPU_SAMPLE_S} tokens, {dt:.1f} s"}
+            "sample": f"fp64 oracle fwd+bwd of head 0's causal prefix of {CPU_SAMPLE_S} tokens, {dt:.1f} s",
+            "extrapolated_full_step_s": step_flop(B, H, S, D) * dt / cflop,
+            "extrapolated_note": "extrapolated: the full step's FLOPs at the sample's rate"}
     print(json.dumps(line), flush=True)
     return 0
 
