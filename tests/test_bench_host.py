@@ -1,0 +1,47 @@
+"""Host-side logic of bench.py, on the CPU: the FLOP convention, the input
+checksums, and the lookup of recorded DRAM traffic, which must return a
+figure only while the kernel's sources still hash as they did at capture."""
+
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_flop_convention():
+    # forward 4·B·H·S²·D/2, backward 2.5 × forward, step 3.5 × forward
+    assert bench.fwd_flop(1, 32, 32768, 128) == 2.0 * 32 * 32768 ** 2 * 128
+    assert abs(bench.fwd_flop(1, 32, 32768, 128) - 8.80e12) < 0.01e12
+    assert bench.step_flop(2, 3, 100, 128) == 3.5 * bench.fwd_flop(2, 3, 100, 128)
+
+
+def test_input_checksums_sum_the_first_2_20_elements():
+    big = torch.ones((1 << 20) + 1000, dtype=torch.bfloat16).view(1, -1, 1, 1)
+    small = torch.arange(10, dtype=torch.float32).to(torch.bfloat16)
+    got = bench.input_checksums((("big", big), ("small", small)))
+    assert got == {"big": float(1 << 20), "small": 45.0}
+
+
+def test_recorded_traffic_needs_matching_source_hash(tmp_path, monkeypatch):
+    csrc = tmp_path / "long_context_causal_blockwise_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name, text in (("attn_bwd.cu", "kernel v1\n"), ("common.cuh", "common\n"), ("tmem_ldst.cuh", "tmem\n")):
+        (csrc / name).write_text(text)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.kernel_source_hash(bench.KERNEL_SOURCES["bwd_fused"])
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "dram_traffic_b1h32s32768.txt").write_text(
+        "# comment lines and prose are skipped\n"
+        f"bwd_fused {h} 2653056256\n"
+        "dq_untile 0123456789abcdef 769436928\n")
+    assert bench.recorded_traffic("bwd_fused") == 2653056256
+    assert bench.recorded_traffic("dq_untile") is None  # recorded for other sources
+    assert bench.recorded_traffic("attn_fwd") is None   # its sources are missing here
+    (csrc / "attn_bwd.cu").write_text("kernel v2\n")
+    assert bench.recorded_traffic("bwd_fused") is None  # the kernel changed since the capture
