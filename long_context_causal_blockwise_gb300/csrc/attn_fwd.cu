@@ -44,6 +44,7 @@ constexpr uint32_t kSmQ = 0;                    // Q_0, Q_1
 constexpr uint32_t kSmKV = 2 * kTileBytes;      // ring
 constexpr uint32_t kSmBar = kSmKV + kStages * kTileBytes;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
+constexpr int kHeadGroup = 4;                   // (b, h) pairs whose query blocks interleave in the CTA order
 
 struct Bars {
   uint64_t q_full;
@@ -113,18 +114,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = static_cast<int>(lane_id());
 
   // Work item: the task owning this CTA, then query block qblk of (b, h) in it.
-  // Tasks come heaviest first; within a task, head-major order (the K/V tiles
-  // every running CTA streams stay in L2), the heaviest (latest) query blocks
-  // of a head first. Row indices below are task-local; q_off / k_off place
-  // them in the shared tensors.
+  // Tasks come heaviest first. Within a task, (b, h) pairs go in groups of
+  // kHeadGroup: a group's CTAs come heaviest (latest) query block first with
+  // its heads interleaved. The running CTAs then stream the K/V tiles of a few
+  // heads only (they stay in L2), and the light blocks of every group finish
+  // the grid rather than one head's light blocks after the others' heavy ones.
+  // Row indices below are task-local; q_off / k_off place them in the shared
+  // tensors.
   int ti = 0;
   while (ti + 1 < p.n_tasks && static_cast<int>(blockIdx.x) >= p.task[ti + 1].cta0) ++ti;
   const int Sq = p.task[ti].q_len, Sk = p.task[ti].k_len, causal = p.task[ti].causal;
   const int q_off = p.task[ti].q_off, k_off = p.task[ti].k_off, o_mode = p.task[ti].o_mode;
   const int local = static_cast<int>(blockIdx.x) - p.task[ti].cta0;
   const int nq = (Sq + 2 * kBM - 1) / (2 * kBM);
-  const int bh = local / nq;
-  const int qblk = nq - 1 - local % nq;
+  const int group = local / (nq * kHeadGroup);
+  const int g0 = group * kHeadGroup;                     // first (b, h) of the group
+  const int gsz = min(kHeadGroup, p.B * p.H - g0);       // the last group may be smaller
+  const int within = local - group * nq * kHeadGroup;    // [0, nq * gsz)
+  const int bh = g0 + within % gsz;
+  const int qblk = nq - 1 - within / gsz;
   const int b = bh / p.H;
   const int h = bh % p.H;
   const int q0 = qblk * 2 * kBM;
