@@ -12,6 +12,15 @@ backward 2.5 x forward, step 7*B*H*S^2*D.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+The line also carries, at N = 1, a "sizes" record (S = 131072 H32, S = 262144
+H40, S = 524288 H32 with RoPE theta 1e6 on Q and K: fwd and bwd ms, TFLOP/s,
+fractions of the tensor peak) and the zigzag ring emulation against monolithic
+attention at S = 131072, P = 8. Fractions use the measured burst bf16 peak
+unless a timed region ran for seconds under the power cap (then the sustained
+figure, as it was measured). After the timed loops the device status word is
+read: a bounded wait that expired inside a kernel (its outputs then
+unfinished) makes the run exit 3, with the word in "device_status".
+
 With N > 1 (torchrun, one rank per GPU) every rank runs its own layer (the
 path shards by independent problems, no collective); value is the whole
 job's FLOP / the slowest rank's time. One JSON line is printed by rank 0.
@@ -119,7 +128,8 @@ def recorded_traffic(kernel):
 
 
 def load_peaks():
-    """(tensor TFLOP/s sustained, tensor burst, HBM GB/s, source)."""
+    """Dense bf16 tensor peaks (burst, sustained) in TFLOP/s, HBM copy GB/s, and
+    where they come from: the measured file, else the fallback figures."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
@@ -127,9 +137,19 @@ def load_peaks():
         burst = float(pk.get("bf16_tflops"))
         sus = float(pk.get("bf16_tflops_sustained", burst))
         hbm = float(pk.get("hbm_gbs"))
-        return sus, burst, hbm, "measured"
+        return {"burst": burst, "sustained": sus, "hbm": hbm, "source": "measured"}
     except Exception:
-        return 1700.0, 1900.0, 6800.0, "fallback"
+        return {"burst": 1900.0, "sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+def tensor_peak(peaks, timed_s, clocks):
+    """The tensor peak that applies to a timed region: the burst figure (a
+    short burst at full clocks), or the sustained one when the region ran for
+    seconds under the power cap, as that figure was measured."""
+    capped = "sw_power_cap" in (clocks or {}).get("reasons", [])
+    if timed_s > 2.0 and capped:
+        return peaks["sustained"], "sustained"
+    return peaks["burst"], "burst"
 
 
 class ClockSampler:
@@ -248,6 +268,8 @@ def run_ours(args, rank, world, local_rank):
     scale = D ** -0.5
     q, k, v, do = gaussian_qkvdo(B, H, S, D, seed=rank, device=dev)
     checksums = input_checksums((("q", q), ("k", k), ("v", v), ("do", do)))
+    # the oracle's sample (head 0's causal prefix), kept on the host for the cpu_baseline leg
+    q_cpu, k_cpu, v_cpu, do_cpu = (t[:, :CPU_SAMPLE_S, :1].cpu() for t in (q, k, v, do))
     o = torch.empty_like(q)
     lse = torch.empty(B, H, S, device=dev)
     delta = torch.empty(B, H, S, device=dev)
@@ -303,11 +325,127 @@ def run_ours(args, rank, world, local_rank):
             per[n].append(evs[j].elapsed_time(evs[j + 1]) / 1e3)
     avg = {n: sum(v_) / len(v_) for n, v_ in per.items()}
 
-    # ---------------- end to end through the public calls, host buffers in and out
-    # Every step copies its own inputs in from pinned host memory and its
-    # results out, inside the timed region. Two device buffer sets and two copy
-    # streams let step i+1's inputs arrive and step i-1's results leave while
-    # step i computes, as a training loop would overlap them.
+    status_bits, status_where = lcb.take_device_status()  # a bounded wait that expired in the timed loop
+    e2e = None if args.no_e2e else run_e2e(args, world, dev, q, k, v, do, o, lse, dq, dk, dv)
+    if e2e is not None:
+        b2, w2 = lcb.take_device_status()  # ... or in the end-to-end leg
+        status_bits |= b2
+        status_where = status_where or w2
+
+    if rank != 0:
+        return 0 if status_bits == 0 else 3
+
+    peaks = load_peaks()
+    hbm, src = peaks["hbm"], peaks["source"]
+    peak, peak_kind = tensor_peak(peaks, t_max, clocks)
+    flop = step_flop(B, H, S, D)
+    value = whole_job_tflops(world, flop, args.steps, t_max)
+    ms = 1e3 * t_max / args.steps
+    pairs = B * H * S * S / 2.0  # causal (query, key) pairs, the R5 convention
+    tiles_bytes = B * H * ((S + 127) // 128) * 128 * D * 4
+    alg = {  # algorithmic work per launch
+        "attn_fwd": ("tensor", 4 * D * pairs),            # S = QK^T and O += PV
+        "bwd_fused": ("tensor", 10 * D * pairs),          # S^T, dP^T, dV, dK, dQ
+        "bwd_preprocess": ("hbm", 2 * B * S * H * D * 2 + B * S * H * 4),
+        "dq_zero": ("hbm", tiles_bytes),                  # async memset of the tiled accumulator
+        "dq_untile": ("hbm", tiles_bytes + B * S * H * D * 2),
+    }
+    kernels = {}
+    for n in names:
+        kind, work = alg[n]
+        t = avg[n]
+        if kind == "tensor":
+            ach = work / t / 1e12
+            kernels[n] = {"ms": 1e3 * t, "tflops": ach, "frac_of_peak": ach / peak,
+                          "frac_of_sustained": ach / peaks["sustained"]}
+        else:
+            ach = work / t / 1e9
+            kernels[n] = {"ms": 1e3 * t, "gbs": ach, "frac_of_peak": ach / hbm}
+    dom = max(names, key=lambda n: avg[n])
+    kind, work = alg[dom]
+    if kind == "tensor":
+        ach = work / avg[dom] / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "frac_of_sustained": ach / peaks["sustained"],
+                "traffic": recorded_traffic(dom) if (H, S) == (32, 32768) else None,
+                "peak_source": f"{src} bf16 {peak_kind} (cuBLAS bf16 GEMM)",
+                "work_per_launch": f"{work:.4e} FLOP = 10*D FLOP x {pairs:.4e} causal pairs"}
+    else:
+        ach = work / avg[dom] / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": recorded_traffic(dom) if (H, S) == (32, 32768) else None,
+                "peak_source": f"{src} HBM copy"}
+    fwd_t = avg["attn_fwd"]
+    bwd_t = sum(avg[n] for n in names if n != "attn_fwd")
+    fwd_tf = fwd_flop(B, H, S, D) / fwd_t / 1e12
+    bwd_tf = 2.5 * fwd_flop(B, H, S, D) / bwd_t / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "S": S, "D": D, "causal": True, "l2": L2_NOTE,
+                   "global_batch": world, "seq_len": S, "parallelism": f"dp{world} (one independent layer per GPU)",
+                   "input_checksum_f64": checksums},
+        "pct_of_peak": 100.0 * (value / world) / peak,
+        "peak_tflops": peak, "peak_kind": peak_kind, "peak_source": f"{src} bf16 {peak_kind}",
+        "peak_tflops_sustained": peaks["sustained"], "pct_of_sustained": 100.0 * (value / world) / peaks["sustained"],
+        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+        "fwd_frac_of_peak": fwd_tf / peak, "bwd_frac_of_peak": bwd_tf / peak,
+        "kernels": kernels,
+        "roofline": roof,
+        "gpu_launches": 4 * args.steps,  # attn_fwd, bwd_preprocess, bwd_fused, dq_untile (dq_zero is a memset)
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_sizes:
+        del q, k, v, do, o, lse, delta, dq, dk, dv, dq_tiles
+        torch.cuda.empty_cache()
+        sampler = ClockSampler(local_rank)
+        sampler.start()
+        time.sleep(0.3)
+        sizes = [size_record(h_, s_, args.size_steps, args.warmup, theta, local_rank)
+                 for h_, s_, theta in ((32, 131072, None), (40, 262144, None), (32, 524288, 1e6))]
+        ring = zigzag_record(args.warmup, args.size_steps, local_rank)
+        sclocks = sampler.stop()
+        for rec in sizes:
+            pk, kind_ = tensor_peak(peaks, rec["timed_s"], sclocks)
+            rec.update({"peak_tflops": pk, "peak_kind": kind_, "fwd_frac_of_peak": rec["fwd_tflops"] / pk,
+                        "bwd_frac_of_peak": rec["bwd_tflops"] / pk, "pct_of_peak": 100.0 * rec["tflops"] / pk,
+                        "fwd_frac_of_burst": rec["fwd_tflops"] / peaks["burst"],
+                        "bwd_frac_of_burst": rec["bwd_tflops"] / peaks["burst"]})
+        line["sizes"] = sizes
+        line["zigzag_ring"] = ring
+        line["sizes_clocks"] = sclocks
+        b2, w2 = lcb.take_device_status()
+        status_bits |= b2
+        status_where = status_where or w2
+    line["device_status"] = status_bits
+    if status_bits:
+        line["device_status_where"] = status_where
+    if world == 1 and not args.no_cpu_baseline:
+        dt, cflop = cpu_oracle_sample(q_cpu, k_cpu, v_cpu, do_cpu, CPU_SAMPLE_S)
+        line["cpu_baseline"] = {
+            "value": cflop / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd of head 0's causal prefix of {CPU_SAMPLE_S} tokens, {dt:.1f} s",
+            "extrapolated_full_step_s": step_flop(B, H, S, D) * dt / cflop,
+            "extrapolated_note": "extrapolated: the full step's FLOPs at the sample's rate"}
+    print(json.dumps(line), flush=True)
+    return 0 if status_bits == 0 else 3
+
+
+def run_e2e(args, world, dev, q, k, v, do, o, lse, dq, dk, dv):
+    """The step end to end through the public calls attn_fwd and attn_bwd with
+    host buffers in and out: every step copies its own inputs in from pinned
+    host memory and its results out, inside the timed region. Two device
+    buffer sets and two copy streams let step i+1's inputs arrive and step
+    i-1's results leave while step i computes, as a training loop would
+    overlap them."""
+    import torch
+
+    import long_context_causal_blockwise_gb300 as lcb
+
+    scale = D ** -0.5
     e2e_steps = max(4, args.steps)  # as many steps as the device-timed run: the pipeline's fill and drain amortise alike
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
     hq, hk, hv, hdo = (pin(t) for t in (q, k, v, do))
@@ -362,85 +500,66 @@ def run_ours(args, rank, world, local_rank):
     ddq = (hdq.to(dev).float() - dq.float()).abs().max().item()
     same = bool(torch.equal(ho.to(dev), o) and torch.equal(hdk.to(dev), dk) and torch.equal(hdv.to(dev), dv)
                 and ddq <= 2 ** -7 * dq.float().abs().max().item())
-
-    if rank != 0:
-        return 0
-
-    sus, burst, hbm, src = load_peaks()
-    flop = step_flop(B, H, S, D)
-    value = whole_job_tflops(world, flop, args.steps, t_max)
-    ms = 1e3 * t_max / args.steps
-    pairs = B * H * S * S / 2.0  # causal (query, key) pairs, the R5 convention
-    tiles_bytes = B * H * ((S + 127) // 128) * 128 * D * 4
-    alg = {  # algorithmic work per launch
-        "attn_fwd": ("tensor", 4 * D * pairs),            # S = QK^T and O += PV
-        "bwd_fused": ("tensor", 10 * D * pairs),          # S^T, dP^T, dV, dK, dQ
-        "bwd_preprocess": ("hbm", 2 * B * S * H * D * 2 + B * S * H * 4),
-        "dq_zero": ("hbm", tiles_bytes),                  # async memset of the tiled accumulator
-        "dq_untile": ("hbm", tiles_bytes + B * S * H * D * 2),
-    }
-    kernels = {}
-    for n in names:
-        kind, work = alg[n]
-        t = avg[n]
-        if kind == "tensor":
-            ach = work / t / 1e12
-            kernels[n] = {"ms": 1e3 * t, "tflops": ach, "frac_of_peak": ach / sus}
-        else:
-            ach = work / t / 1e9
-            kernels[n] = {"ms": 1e3 * t, "gbs": ach, "frac_of_peak": ach / hbm}
-    dom = max(names, key=lambda n: avg[n])
-    kind, work = alg[dom]
-    if kind == "tensor":
-        ach = work / avg[dom] / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": sus, "unit": "TFLOP/s", "frac": ach / sus,
-                "traffic": recorded_traffic(dom) if (H, S) == (32, 32768) else None,
-                "peak_source": f"{src} bf16 sustained"}
-    else:
-        ach = work / avg[dom] / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "traffic": recorded_traffic(dom) if (H, S) == (32, 32768) else None,
-                "peak_source": f"{src} HBM copy"}
-    fwd_t = avg["attn_fwd"]
-    bwd_t = sum(avg[n] for n in names if n != "attn_fwd")
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "H": H, "S": S, "D": D, "causal": True, "l2": L2_NOTE,
-                   "global_batch": world, "seq_len": S, "parallelism": f"dp{world} (one independent layer per GPU)",
-                   "input_checksum_f64": checksums},
-        "pct_of_peak": 100.0 * (value / world) / sus,
-        "peak_tflops": sus, "peak_source": f"{src} bf16 sustained",
-        "fwd_tflops": fwd_flop(B, H, S, D) / fwd_t / 1e12,
-        "bwd_tflops": 2.5 * fwd_flop(B, H, S, D) / bwd_t / 1e12,
-        "fwd_frac_of_peak": fwd_flop(B, H, S, D) / fwd_t / 1e12 / sus,
-        "bwd_frac_of_peak": 2.5 * fwd_flop(B, H, S, D) / bwd_t / 1e12 / sus,
-        "kernels": kernels,
-        "roofline": roof,
-        "e2e": {"value": whole_job_tflops(world, flop, 1, e2e_t), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_t, "steps": e2e_steps,
-                "matches_device_run": same,
-                "overlap": "step i+1's host-to-device and step i-1's device-to-host copies run on two copy "
-                           "streams during step i (double-buffered device tensors)"},
-        "gpu_launches": 4 * args.steps,  # attn_fwd, bwd_preprocess, bwd_fused, dq_untile (dq_zero is a memset)
-        "clocks": clocks,
-    }
-    if world == 1 and not args.no_cpu_baseline:
-        dt, cflop = cpu_oracle_sample(q, k, v, do, CPU_SAMPLE_S)
-        line["cpu_baseline"] = {
-            "value": cflop / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd of head 0's causal prefix of {CPU_SAMPLE_S} tokens, {dt:.1f} s",
-            "extrapolated_full_step_s": step_flop(B, H, S, D) * dt / cflop,
-            "extrapolated_note": "extrapolated: the full step's FLOPs at the sample's rate"}
-    print(json.dumps(line), flush=True)
-    return 0
+    del dev_in, dev_out, ws
+    torch.cuda.empty_cache()
+    return {"value": whole_job_tflops(world, step_flop(B, H, S, D), 1, e2e_t), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_t, "steps": e2e_steps,
+            "matches_device_run": same,
+            "overlap": "step i+1's host-to-device and step i-1's device-to-host copies run on two copy "
+                       "streams during step i (double-buffered device tensors)"}
 
 
-def run_zigzag(args):
-    """Times the one-device zigzag ring (S = 131072, P = 8, H = 32) against
-    monolithic attention on the same inputs; prints one JSON line (not the
-    headline bench line)."""
+def size_record(h, s, steps, warmup, rope_theta, local_rank):
+    """One size of the metric's range: attn_fwd and attn_bwd (the public calls,
+    workspace passed in) timed separately per step with CUDA events."""
+    import torch
+
+    import long_context_causal_blockwise_gb300 as lcb
+    from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo
+
+    dev = torch.device("cuda", local_rank)
+    scale = D ** -0.5
+    q, k, v, do = gaussian_qkvdo(1, h, s, D, seed=0, device=dev)
+    if rope_theta:  # positions 0..S-1, outside the timed region
+        lcb.rope(q, rope_theta)
+        lcb.rope(k, rope_theta)
+    o, lse = torch.empty_like(q), torch.empty(1, h, s, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(lcb.attn_bwd_workspace_bytes(1, h, s, D), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        lcb.attn_fwd(q, k, v, causal=True, scale=scale, o=o, lse=lse)
+
+    def bwd():
+        lcb.attn_bwd(q, k, v, o, lse, do, causal=True, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in evs:
+        e[0].record(stream)
+        fwd()
+        e[1].record(stream)
+        bwd()
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    tf = sum(e[0].elapsed_time(e[1]) for e in evs) / steps / 1e3
+    tb = sum(e[1].elapsed_time(e[2]) for e in evs) / steps / 1e3
+    ff = fwd_flop(1, h, s, D)
+    del q, k, v, do, o, lse, dq, dk, dv, ws
+    torch.cuda.empty_cache()
+    return {"workload": f"B1 H{h} S{s} D128 causal" + (f", Q/K RoPE theta={rope_theta:g}" if rope_theta else ""),
+            "H": h, "S": s, "steps": steps, "warmup": warmup, "fwd_ms": 1e3 * tf, "bwd_ms": 1e3 * tb,
+            "ms_per_step": 1e3 * (tf + tb), "tflops": 3.5 * ff / (tf + tb) / 1e12,
+            "fwd_tflops": ff / tf / 1e12, "bwd_tflops": 2.5 * ff / tb / 1e12, "timed_s": steps * (tf + tb)}
+
+
+def zigzag_record(warmup, steps, local_rank, detail=False):
+    """The one-device zigzag ring (S = 131072, P = 8, H = 32) against monolithic
+    attention on the same inputs, fwd+bwd per step, CUDA events."""
     import torch
 
     import long_context_causal_blockwise_gb300 as lcb
@@ -448,8 +567,7 @@ def run_zigzag(args):
     from long_context_causal_blockwise_gb300.zigzag import ZigzagPlan
 
     Hz, Sz, Pz = 32, 131072, 8
-    dev = torch.device("cuda", 0)
-    lcb.load()
+    dev = torch.device("cuda", local_rank)
     q, k, v, do = gaussian_qkvdo(1, Hz, Sz, D, seed=0, device=dev)
     plan = ZigzagPlan(Sz, Pz, dev)
     c2 = Sz // Pz
@@ -462,11 +580,10 @@ def run_zigzag(args):
     g16 = tuple(torch.empty_like(q) for _ in range(3))
     delta = torch.empty(1, Hz, Sz, device=dev)
     qz, kz, vz, doz = (plan.gather(x) for x in (q, k, v, do))
+    tiles = lcb.dq_tiles_zeros(1, Hz, Sz, dev)
 
     def ring_fwd(fused=True):
         return lcb.zigzag_attention_fwd(qz, kz, vz, plan, fused=fused, **bufs)
-
-    tiles = lcb.dq_tiles_zeros(1, Hz, Sz, dev)
 
     def ring():
         o, lse, _ = ring_fwd()
@@ -480,39 +597,58 @@ def run_zigzag(args):
         lcb.attn_fwd(q, k, v, o=o_m, lse=lse_m)
         lcb.attn_bwd(q, k, v, o_m, lse_m, do, dq=dq, dk=dk, dv=dv, workspace=ws)
 
-    def timed(fn, steps):
-        for _ in range(args.warmup):
+    def timed(fn, n):
+        for _ in range(warmup):
             fn()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(steps):
+        for _ in range(n):
             fn()
         e1.record()
         torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / steps
+        return e0.elapsed_time(e1) / n
 
-    steps = max(1, min(args.steps, 5))
     t_ring, t_mono = timed(ring, steps), timed(mono, steps)
-    t_fwd_fused, t_fwd_unfused = timed(ring_fwd, steps), timed(lambda: ring_fwd(False), steps)
-    t_fwd_mono = timed(lambda: lcb.attn_fwd(q, k, v, o=o_m, lse=lse_m), steps)
-    # merge kernel alone: one LOWER/UPPER-sized merge (2c rows) timed in isolation
-    oa, la = bufs["o_acc"][:, :c2], bufs["lse"][:, :, :c2]
-    ob, lb = bufs["o_blk"], bufs["lse_blk"]
-    t_merge = timed(lambda: lcb.attn_lse_merge(oa, la, ob, lb), 20)
-    merge_bytes = c2 * Hz * (D * 4 * 2 + D * 2 + 12)
-    _, _, hbm, src = load_peaks()
     flop = step_flop(1, Hz, Sz, D)
-    print(json.dumps({
-        "metric": "zigzag ring emulation fwd+bwd (P=8, S=131072, H=32, D=128) vs monolithic",
-        "ring_ms": t_ring, "monolithic_ms": t_mono, "ring_overhead_pct": 100.0 * (t_ring / t_mono - 1.0),
-        "ring_tflops": flop / t_ring / 1e9, "monolithic_tflops": flop / t_mono / 1e9,
-        "fwd_ms": {"ring_fused_merge": t_fwd_fused, "ring_merge_kernel": t_fwd_unfused, "monolithic": t_fwd_mono},
-        "merge_ms_per_call": t_merge, "merge_rows": c2, "merge_gbs": merge_bytes / t_merge / 1e6,
-        "merge_frac_of_hbm": merge_bytes / t_merge / 1e6 / hbm, "hbm_peak_source": src,
-        "launches_per_ring_step": "fwd: 1 grouped launch of the P tasks (merge fused in the epilogue); bwd: 1 grouped one-pass launch of the P tasks; + preprocess, zeroing and untile once per pass"}),
-          flush=True)
-    return 0
+    rec = {"workload": "zigzag ring emulation fwd+bwd, P=8 virtual ranks, B1 H32 S131072 D128, vs monolithic",
+           "steps": steps, "warmup": warmup, "ring_ms": t_ring, "monolithic_ms": t_mono,
+           "ring_overhead_pct": 100.0 * (t_ring / t_mono - 1.0),
+           "ring_tflops": flop / t_ring / 1e9, "monolithic_tflops": flop / t_mono / 1e9}
+    if detail:
+        t_fwd_fused, t_fwd_unfused = timed(ring_fwd, steps), timed(lambda: ring_fwd(False), steps)
+        t_fwd_mono = timed(lambda: lcb.attn_fwd(q, k, v, o=o_m, lse=lse_m), steps)
+        # merge kernel alone: one LOWER/UPPER-sized merge (2c rows) timed in isolation
+        oa, la = bufs["o_acc"][:, :c2], bufs["lse"][:, :, :c2]
+        ob, lb = bufs["o_blk"], bufs["lse_blk"]
+        t_merge = timed(lambda: lcb.attn_lse_merge(oa, la, ob, lb), 20)
+        merge_bytes = c2 * Hz * (D * 4 * 2 + D * 2 + 12)
+        hbm = load_peaks()["hbm"]
+        rec.update({
+            "fwd_ms": {"ring_fused_merge": t_fwd_fused, "ring_merge_kernel": t_fwd_unfused,
+                       "monolithic": t_fwd_mono},
+            "merge_ms_per_call": t_merge, "merge_rows": c2, "merge_gbs": merge_bytes / t_merge / 1e6,
+            "merge_frac_of_hbm": merge_bytes / t_merge / 1e6 / hbm,
+            "launches_per_ring_step": "fwd: 1 grouped launch of the P tasks (merge fused in the epilogue); bwd: 1 "
+                                      "grouped one-pass launch of the P tasks; + preprocess, zeroing and untile "
+                                      "once per pass"})
+    del q, k, v, do, qz, kz, vz, doz, bufs, g32, g16, delta, tiles, o_m, lse_m, dq, dk, dv, ws
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_zigzag(args):
+    """Times the one-device zigzag ring against monolithic attention; prints one
+    JSON line (not the headline bench line)."""
+    import long_context_causal_blockwise_gb300 as lcb
+
+    lcb.load()
+    rec = zigzag_record(args.warmup, max(1, min(args.steps, 5)), 0, detail=True)
+    rec["metric"] = "zigzag ring emulation fwd+bwd (P=8, S=131072, H=32, D=128) vs monolithic"
+    bits, _ = lcb.take_device_status()
+    rec["device_status"] = bits
+    print(json.dumps(rec), flush=True)
+    return 0 if bits == 0 else 3
 
 
 def run_rope(args):
@@ -611,6 +747,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg (its double-buffered tensors; for small ncu captures)")
+    ap.add_argument("--no-sizes", action="store_true",
+                    help="skip the S=128K-512K sizes and the zigzag ring record (for ncu captures)")
+    ap.add_argument("--size-steps", type=int, default=3, help="timed steps per size of the sizes record")
     ap.add_argument("--H", type=int, default=H, help="heads (profiling of smaller cases only)")
     ap.add_argument("--S", type=int, default=S, help="sequence length (profiling of smaller cases only)")
     ap.add_argument("--vocab", type=int, default=32000, help="vocabulary size of --ce")

@@ -165,8 +165,9 @@ size_t attn_bwd_workspace_bytes(int B, int H, int S, int D);
  * Delta = rowsum(dO * O) preprocess, zeroes the tiled fp32 dQ accumulator in
  * the workspace, runs the fused pass (attn_bwd_fused_ex) and converts dQ to
  * bf16 (lcb_dq_untile).
- * dQ's fp32 summation order is not fixed (atomic adds), so repeated calls may
- * differ in the last bits of dq; dk and dv are deterministic.
+ * dQ's fp32 summation order is not fixed (the partials of many CTAs are added
+ * into the accumulator by asynchronous bulk reductions in L2), so repeated
+ * calls may differ in the last bits of dq; dk and dv are deterministic.
  * workspace: device memory of at least attn_bwd_workspace_bytes(), 16-byte
  * aligned, owned by the caller, contents ignored.
  */
@@ -382,19 +383,24 @@ int lcb_take_device_status(unsigned int* where);
  * because their memory plan is fixed at start-up, or because they must not
  * call cudaMalloc, which can synchronise the device mid-pipeline.
  * Same arguments and results as attn_bwd minus the workspace. The Delta
- * scratch lives in a fixed 8 MiB array in device memory inside the library;
- * every GPU that loads the library holds it until the process exits.
+ * scratch lives in a fixed 8 MiB array in device memory inside the library.
  *  - Limit: B * H * S <= attn_bwd_noalloc_max_rows() (2^21); larger problems
  *    return LCB_ERR_SCRATCH and launch nothing.
- *  - No allocation: the call makes no cudaMalloc/cudaFree or other
- *    allocating call. Its first call on a device looks up the array's device
- *    address (once per device); make that first call before any stream
- *    capture.
- *  - Sharing: every call uses the same array, which keeps the previous
- *    call's contents. The call overwrites all the Delta values it reads, so
- *    nothing needs clearing, but calls that overlap on the GPU (different
- *    streams, or devices sharing nothing else) race on the array: order them
- *    on one stream.
+ *  - First call on a device: CUDA loads modules lazily by default, so the
+ *    first call on each device (in each context, after a cudaDeviceReset too)
+ *    loads the library's module there, which reserves the 8 MiB array and may
+ *    synchronise the device. Make that first call outside any stream capture.
+ *    The array then stays reserved until the process exits or the context is
+ *    reset.
+ *  - No allocation after that: later calls make no cudaMalloc/cudaFree or
+ *    other allocating call; each looks up the array's device address, which
+ *    allocates nothing once the module is loaded.
+ *  - Sharing: the array exists once per device. Every call on one device uses
+ *    it and it keeps the previous call's contents; the call writes all the
+ *    Delta values it reads before reading them, so nothing needs clearing.
+ *    Calls that overlap on the GPU of the same device (issued on different
+ *    streams without ordering) race on the array; calls ordered on one stream
+ *    are safe, and calls on different devices each use their own copy.
  */
 int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                      void* dq, void* dk, void* dv, int B, int H, int S, int D, int causal, float scale,

@@ -19,12 +19,9 @@ namespace lcb {
 namespace {
 
 constexpr int kHeadDim = 128;
-constexpr int kMaxDevices = 64;
 
 __device__ uint32_t g_status_words[4];
 
-uint32_t* g_status_ptr[kMaxDevices] = {};
-std::mutex g_mu;
 
 unsigned long long env_wait_limit() {
   const char* s = std::getenv("LCB_WAIT_LIMIT_NS");
@@ -45,18 +42,27 @@ bool checked_mode() {
   return on;
 }
 
-// Device address of the status word on the current device (set-up once per device).
+// Device address of the status word in the current device's context. Looked
+// up on every call rather than cached: a context torn down by
+// cudaDeviceReset and created again may place the word elsewhere.
 int status_words(uint32_t** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LCB_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_words) != cudaSuccess) return LCB_ERR_CUDA;
-    g_status_ptr[dev] = static_cast<uint32_t*>(p);
-  }
-  *out = g_status_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status_words) != cudaSuccess || p == nullptr) return LCB_ERR_CUDA;
+  *out = static_cast<uint32_t*>(p);
   return LCB_OK;
+}
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <class Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
 }
 
 int dev_status(DevStatus* st) {
@@ -123,6 +129,29 @@ int make_tma_map_bf16(CUtensorMap* map, const RowView& v, int B, int rows, int H
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? LCB_OK : LCB_ERR_ARG;
+}
+
+unsigned long long current_context_id() {
+  static const CtxGetCurrentFn get_cur = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_cur || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+int set_smem_limit_once(DeviceOnce& once, const void* kernel, int bytes) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LCB_ERR_CUDA;
+  return once.run(
+      dev, current_context_id(),
+      [&] {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess
+                   ? LCB_OK
+                   : LCB_ERR_CUDA;
+      },
+      LCB_ERR_CUDA);
 }
 
 }  // namespace lcb

@@ -1131,13 +1131,8 @@ int launch_attn_bwd_dkdv(const BwdLaunch& a, cudaStream_t stream) {
     if ((rc = make_tma_map_bf16(&tq, a.q, a.B, a.Sq, a.H * kD, kT)) != 0) return rc;
     if ((rc = make_tma_map_bf16(&tdo, a.dO, a.B, a.Sq, a.H * kD, kT)) != 0) return rc;
   }
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem) !=
-        cudaSuccess)
-      return -4;
-    attr = true;
-  }
+  static DeviceOnce smem_set;
+  if ((rc = set_smem_limit_once(smem_set, reinterpret_cast<const void*>(attn_bwd_dkdv_kernel), kKvSmem)) != 0) return rc;
   Params p = base_params(a);
   p.g0 = a.dk;
   p.g1 = a.dv;
@@ -1159,13 +1154,8 @@ int launch_attn_bwd_fused(const BwdLaunch& a, const BwdTask* tasks, int n_tasks,
   if ((rc = make_tma_map_bf16(&tv, a.v, a.B, k_rows, a.H * kD, kT)) != 0) return rc;
   if ((rc = make_tma_map_bf16(&tq, a.q, a.B, q_rows, a.H * kD, kT)) != 0) return rc;
   if ((rc = make_tma_map_bf16(&tdo, a.dO, a.B, q_rows, a.H * kD, kT)) != 0) return rc;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_bwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFuSmem) !=
-        cudaSuccess)
-      return -4;
-    attr = true;
-  }
+  static DeviceOnce smem_set;
+  if ((rc = set_smem_limit_once(smem_set, reinterpret_cast<const void*>(attn_bwd_fused_kernel), kFuSmem)) != 0) return rc;
   Params p = base_params(a);
   p.g0 = a.dk;
   p.g1 = a.dv;
@@ -1242,13 +1232,8 @@ int launch_attn_bwd_dq(const BwdLaunch& a, cudaStream_t stream) {
     if ((rc = make_tma_map_bf16(&tk, a.k, a.B, a.Sk, a.H * kD, kT)) != 0) return rc;
     if ((rc = make_tma_map_bf16(&tv, a.v, a.B, a.Sk, a.H * kD, kT)) != 0) return rc;
   }
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
-        cudaSuccess)
-      return -4;
-    attr = true;
-  }
+  static DeviceOnce smem_set;
+  if ((rc = set_smem_limit_once(smem_set, reinterpret_cast<const void*>(attn_bwd_dq_kernel), kQSmem)) != 0) return rc;
   Params p = base_params(a);
   p.f0 = static_cast<const __nv_bfloat16*>(a.q.ptr);
   p.f1 = static_cast<const __nv_bfloat16*>(a.dO.ptr);

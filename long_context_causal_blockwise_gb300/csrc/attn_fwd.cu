@@ -454,13 +454,9 @@ int launch_attn_fwd(const FwdLaunch& a, cudaStream_t stream) {
   if ((rc = make_tma_map_bf16(&tq, a.q, a.B, a.q_rows, a.H * kD, kBM)) != 0) return rc;
   if ((rc = make_tma_map_bf16(&tk, a.k, a.B, a.k_rows, a.H * kD, kBN)) != 0) return rc;
   if ((rc = make_tma_map_bf16(&tv, a.v, a.B, a.k_rows, a.H * kD, kBN)) != 0) return rc;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess)
-      return -4;
-    attr_done = true;
-  }
+  static DeviceOnce smem_set;
+  if ((rc = set_smem_limit_once(smem_set, reinterpret_cast<const void*>(attn_fwd_kernel), kSmemBytes)) != 0)
+    return rc;
   Params p;
   p.o = a.o;
   p.lse = a.lse;

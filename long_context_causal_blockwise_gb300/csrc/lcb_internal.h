@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "device_once.h"
 
 namespace lcb {
 
@@ -21,6 +22,15 @@ struct RowView {
 // 64 (inner, 128 bytes) x box_rows x 1 and 128-byte swizzle.
 // Returns 0 on success, a negative LCB status on failure.
 int make_tma_map_bf16(CUtensorMap* map, const RowView& v, int B, int rows, int HD, int box_rows);
+
+// Id of the calling thread's current CUDA context (unique within the process),
+// or 0 when there is none or the driver cannot tell.
+unsigned long long current_context_id();
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` in the current
+// device's context, the first time it is asked for that context (function
+// attributes belong to a device context). Returns 0, or LCB_ERR_CUDA.
+int set_smem_limit_once(DeviceOnce& once, const void* kernel, int bytes);
 
 // One block of a forward launch (rows relative to the shared tensors).
 struct FwdTask {

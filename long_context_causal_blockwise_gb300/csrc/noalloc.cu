@@ -9,14 +9,15 @@
 // afterwards; code that must not call cudaMalloc because that call can
 // synchronise the device in the middle of an asynchronous pipeline. For them
 // this entry point keeps the scratch in a fixed array in device global
-// memory, compiled into the library. Every GPU that loads the library holds
-// this array until the process exits.
+// memory, compiled into the library. The array is reserved on a device when
+// this file's module is loaded into that device's context: with CUDA's lazy
+// module loading (the default) that happens during the first call of this
+// entry point on the device, and the array is then held until the process
+// exits or the context is reset.
 //
-// The entry point runs the same kernels as attn_bwd: Delta preprocess, then
+// The entry point runs the same kernels as attn_bwd_ex: Delta preprocess, then
 // the dK/dV and dQ passes, with Delta read from the array.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "lcb_attn.h"
 
@@ -24,25 +25,18 @@ namespace {
 
 // Up to this many (batch, head, row) Delta values: 2^21 fp32 = 8 MiB.
 constexpr long long kNoAllocMaxRows = 1LL << 21;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_noalloc_delta[kNoAllocMaxRows];
 
-float* g_scratch_ptr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
-// Device address of the array on the current device; looked up once per
-// device (the host-side name of the array is not a device address).
+// Device address of the array in the current device's context. The host-side
+// name of the array is not a device address. The address is looked up on
+// every call, not cached: after cudaDeviceReset the module is loaded again and
+// the array may sit elsewhere. Once the module is loaded the lookup allocates
+// nothing; the first lookup on a device loads it.
 int scratch_ptr(float** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LCB_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_delta) != cudaSuccess || p == nullptr) return LCB_ERR_CUDA;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_delta) != cudaSuccess || p == nullptr) return LCB_ERR_CUDA;
+  *out = static_cast<float*>(p);
   return LCB_OK;
 }
 

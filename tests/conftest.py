@@ -26,3 +26,21 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def device_status_clear(request):
+    """After every GPU test, no kernel's bounded wait may have expired (a
+    kernel that gives up returns early with its outputs unfinished). The
+    bounded-wait self test reads and clears the word itself."""
+    yield
+    if "gpu" not in request.node.keywords:
+        return
+    import torch
+
+    if not torch.cuda.is_available():
+        return
+    import long_context_causal_blockwise_gb300 as lcb
+
+    bits, where = lcb.take_device_status()
+    assert bits == 0, f"a bounded wait expired during this test: status {bits:#x}, where {where:#x}"

@@ -45,3 +45,24 @@ def test_recorded_traffic_needs_matching_source_hash(tmp_path, monkeypatch):
     assert bench.recorded_traffic("attn_fwd") is None   # its sources are missing here
     (csrc / "attn_bwd.cu").write_text("kernel v2\n")
     assert bench.recorded_traffic("bwd_fused") is None  # the kernel changed since the capture
+
+
+def test_tensor_peak_is_burst_unless_a_long_region_ran_power_capped():
+    peaks = {"burst": 1904.1, "sustained": 1715.4, "hbm": 6743.6, "source": "measured"}
+    # a sub-second region at full clocks: the burst figure
+    assert bench.tensor_peak(peaks, 0.56, {"reasons": []}) == (1904.1, "burst")
+    # the power cap alone in a short region does not change it, nor a long uncapped one
+    assert bench.tensor_peak(peaks, 0.56, {"reasons": ["sw_power_cap"]}) == (1904.1, "burst")
+    assert bench.tensor_peak(peaks, 20.0, {"reasons": []}) == (1904.1, "burst")
+    # seconds under the power cap: the sustained figure, measured that way
+    assert bench.tensor_peak(peaks, 20.0, {"reasons": ["sw_power_cap"]}) == (1715.4, "sustained")
+    assert bench.tensor_peak(peaks, 20.0, None) == (1904.1, "burst")
+
+
+def test_load_peaks_reads_the_measured_file(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_peaks()["source"] == "fallback"
+    (tmp_path / "MEASURED_PEAKS.json").write_text(
+        '{"hbm_gbs": 6743.6, "bf16_tflops": 1904.1, "bf16_tflops_sustained": 1715.4}')
+    pk = bench.load_peaks()
+    assert pk == {"burst": 1904.1, "sustained": 1715.4, "hbm": 6743.6, "source": "measured"}

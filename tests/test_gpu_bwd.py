@@ -231,7 +231,7 @@ def test_fused_pass_adds_into_dq_and_masks_ragged_keys():
 
 
 def test_monolithic_backward_two_calls_agree():
-    """attn_bwd (fused, fp32 atomics for dQ) is repeatable to within bf16
+    """attn_bwd (fused; dQ partials added by bulk reductions in L2) is repeatable to within bf16
     rounding; dK and dV are bit-identical."""
     q, k, v, do = gaussian_qkvdo(1, 4, 1024, D, seed=21)
     o, lse = lcb.attn_fwd(q, k, v)
