@@ -15,7 +15,9 @@ backward 2.5 x forward, step 7*B*H*S^2*D.
 The line also carries, at N = 1, a "sizes" record (S = 131072 H32, S = 262144
 H40, S = 524288 H32 with RoPE theta 1e6 on Q and K: fwd and bwd ms, TFLOP/s,
 fractions of the tensor peak) and the zigzag ring emulation against monolithic
-attention at S = 131072, P = 8. Fractions use the measured burst bf16 peak
+attention at S = 131072, P = 8, and Ulysses over P = 8 emulated ranks at
+the same size (the all-to-all kernel's GB/s, fwd+bwd against monolithic).
+Fractions use the measured burst bf16 peak
 unless a timed region ran for seconds under the power cap (then the sustained
 figure, as it was measured). After the timed loops the device status word is
 read: a bounded wait that expired inside a kernel (its outputs then
@@ -107,6 +109,7 @@ KERNEL_SOURCES = {
     "bwd_preprocess": ("lse_merge.cu", "common.cuh"),
     "rope": ("rope.cu", "common.cuh"),
     "cross_entropy": ("cross_entropy.cu", "common.cuh"),
+    "ulysses_a2a": ("ulysses.cu",),
 }
 
 
@@ -407,6 +410,7 @@ def run_ours(args, rank, world, local_rank):
         sizes = [size_record(h_, s_, args.size_steps, args.warmup, theta, local_rank)
                  for h_, s_, theta in ((32, 131072, None), (40, 262144, None), (32, 524288, 1e6))]
         ring = zigzag_record(args.warmup, args.size_steps, local_rank)
+        uly = ulysses_record(args.warmup, args.size_steps, local_rank)
         sclocks = sampler.stop()
         for rec in sizes:
             pk, kind_ = tensor_peak(peaks, rec["timed_s"], sclocks)
@@ -416,6 +420,7 @@ def run_ours(args, rank, world, local_rank):
                         "bwd_frac_of_burst": rec["bwd_tflops"] / peaks["burst"]})
         line["sizes"] = sizes
         line["zigzag_ring"] = ring
+        line["ulysses"] = uly
         line["sizes_clocks"] = sclocks
         b2, w2 = lcb.take_device_status()
         status_bits |= b2
@@ -635,6 +640,62 @@ def zigzag_record(warmup, steps, local_rank, detail=False):
     del q, k, v, do, qz, kz, vz, doz, bufs, g32, g16, delta, tiles, o_m, lse_m, dq, dk, dv, ws
     torch.cuda.empty_cache()
     return rec
+
+
+def ulysses_record(warmup, steps, local_rank):
+    """Ulysses over P = 8 emulated ranks at B1 H32 S131072: the all-to-all
+    kernel alone (bytes read + written per call against the HBM peak), and
+    Ulysses fwd+bwd (4 all-to-alls in, 4 out, attention on the head layout)
+    against monolithic attention on the same inputs."""
+    import torch
+
+    import long_context_causal_blockwise_gb300 as lcb
+    from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo
+
+    Hu, Su, Pu = 32, 131072, 8
+    dev = torch.device("cuda", local_rank)
+    q, k, v, do = gaussian_qkvdo(1, Hu, Su, D, seed=0, device=dev)
+    qh = torch.empty((Pu, Su, Hu // Pu, D), dtype=q.dtype, device=dev)
+    back = torch.empty_like(q)
+    o_m, lse_m = torch.empty_like(q), torch.empty(1, Hu, Su, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(lcb.attn_bwd_workspace_bytes(Pu, Hu // Pu, Su, D), dtype=torch.uint8, device=dev)
+
+    def timed(fn, n):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    t_in = timed(lambda: lcb.ulysses_all_to_all(q, Pu, to_heads=True, out=qh), 20)
+    t_out = timed(lambda: lcb.ulysses_all_to_all(qh, Pu, to_heads=False, out=back), 20)
+
+    def uly():
+        o, ctx = lcb.ulysses_attention_fwd(q, k, v, Pu)
+        lcb.ulysses_attention_bwd(do, ctx, workspace=ws)
+
+    def mono():
+        lcb.attn_fwd(q, k, v, o=o_m, lse=lse_m)
+        lcb.attn_bwd(q, k, v, o_m, lse_m, do, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    t_u, t_m = timed(uly, steps), timed(mono, steps)
+    nbytes = 2 * q.numel() * q.element_size()
+    hbm = load_peaks()["hbm"]
+    del q, k, v, do, qh, back, o_m, lse_m, dq, dk, dv, ws
+    torch.cuda.empty_cache()
+    return {"workload": "Ulysses all-to-all around attention, P=8 emulated ranks (4 heads each), "
+                        "B1 H32 S131072 D128 causal, vs monolithic",
+            "a2a_ms_seq_to_head": t_in, "a2a_ms_head_to_seq": t_out, "a2a_bytes_per_call": nbytes,
+            "a2a_gbs": nbytes / t_in / 1e6, "a2a_frac_of_hbm": nbytes / t_in / 1e6 / hbm,
+            "a2a_gbs_head_to_seq": nbytes / t_out / 1e6,
+            "ulysses_ms": t_u, "monolithic_ms": t_m, "ulysses_overhead_pct": 100.0 * (t_u / t_m - 1.0),
+            "steps": steps, "warmup": warmup}
 
 
 def run_zigzag(args):

@@ -376,6 +376,29 @@ int lcb_selftest_bounded_wait(void* stream);
 int lcb_take_device_status(unsigned int* where);
 
 /*
+ * lcb_ulysses_all_to_all — the all-to-all of Ulysses sequence parallelism for
+ * P ranks emulated on one device ([SP] §1: Ulysses注意力, based on DeepSpeed;
+ * [ZZ] §模型并行策略解析: ulysses_attn). Rank r of P holds sequence rows
+ * [r S/P, (r+1) S/P) of all heads; rank j after the exchange holds every row
+ * of heads [j H/P, (j+1) H/P).
+ * Layouts (contiguous, elements of elem_bytes bytes, 2 = bf16 or 4 = fp32):
+ *   sequence layout: [B, S, H, D], the P ranks' pieces one after another;
+ *   head layout:     [P, B, S, H/P, D], rank j's part at element offset
+ *                    j * B * S * (H/P) * D. Taken together the parts are one
+ *                    [P*B, S, H/P, D] tensor: a single attention call with
+ *                    batch P*B and H/P heads computes every rank's heads.
+ * direction LCB_ULYSSES_SEQ_TO_HEAD: head[j][b][s][hh] = seq[b][s][j*H/P+hh];
+ * direction LCB_ULYSSES_HEAD_TO_SEQ: the inverse.
+ * A copy (no arithmetic). Requires P | H, P | S, (H/P)*D*elem_bytes a multiple
+ * of 16 bytes, src and dst 16-byte aligned and not overlapping (no in-place),
+ * B*S*(H/P)*D*elem_bytes/16 < 2^31; LCB_ERR_ARG otherwise.
+ */
+#define LCB_ULYSSES_SEQ_TO_HEAD 0
+#define LCB_ULYSSES_HEAD_TO_SEQ 1
+int lcb_ulysses_all_to_all(const void* src, void* dst, int B, int S, int H, int D, int P, int elem_bytes,
+                           int direction, void* stream);
+
+/*
  * attn_bwd_noalloc — attn_bwd for callers that cannot allocate device memory.
  * The source pages have no counterpart of this call; it exists for callers
  * that cannot hand the library a workspace, because their memory manager

@@ -8,7 +8,12 @@ Public calls (all run in this library's CUDA kernels):
   attn_lse_merge, zigzag_schedule, permute_rows, cast_f32_bf16,
   rope (rotary position embedding with a raised base, and its inverse),
   cross_entropy (the loss head with an in-place backward),
-  zigzag_attention_fwd / zigzag_attention_bwd (the one-device zigzag ring).
+  zigzag_attention_fwd / zigzag_attention_bwd (the one-device zigzag ring),
+  ulysses_all_to_all, ulysses_attention_fwd / ulysses_attention_bwd (Ulysses
+  sequence parallelism over P ranks emulated on one device),
+  RingRank / DistRingTransport / LoopbackRing (the rank-local zigzag ring
+  driver: torch.distributed point-to-point between processes, or P ranks in
+  one process).
 
 The shared library is loaded on first use; importing the package does not
 touch the GPU.
@@ -38,6 +43,9 @@ from ._lib import (  # noqa: F401
     selftest_bounded_wait,
     set_wait_limit_ns,
     take_device_status,
+    ulysses_all_to_all,
     zigzag_schedule,
 )
+from .ring import DistRingTransport, LoopbackRing, RingRank, run_rank  # noqa: F401
+from .ulysses import ulysses_attention_bwd, ulysses_attention_fwd  # noqa: F401
 from .zigzag import zigzag_attention_bwd, zigzag_attention_fwd  # noqa: F401

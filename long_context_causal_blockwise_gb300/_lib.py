@@ -83,6 +83,7 @@ _SIGNATURES = {
     "lcb_permute_rows": ([_P, _P, _P, _I, _LL, _P], _I),
     "lcb_scatter_rows": ([_P, _P, _P, _I, _LL, _P], _I),
     "lcb_cast_f32_bf16": ([_P, _P, _LL, _P], _I),
+    "lcb_ulysses_all_to_all": ([_P, _P, _I, _I, _I, _I, _I, _I, _I, _P], _I),
     "lcb_set_wait_limit_ns": ([_U64], _U64),
     "attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P], _I),
     "attn_bwd_noalloc_max_rows": ([], _LL),
@@ -487,6 +488,41 @@ def permute_rows(src, dst, perm_dev, scatter=False):
     fn = load().lcb_scatter_rows if scatter else load().lcb_permute_rows
     _check("permute_rows", fn(_ptr(src), _ptr(dst), _ptr(perm_dev), rows, row_bytes, _stream(src)))
     return dst
+
+
+ULYSSES_SEQ_TO_HEAD, ULYSSES_HEAD_TO_SEQ = 0, 1
+
+
+def ulysses_all_to_all(src, P, to_heads=True, out=None):
+    """The Ulysses all-to-all of P emulated ranks (include/lcb_attn.h).
+
+    to_heads=True: src is a contiguous [B, S, H, D] tensor (the ranks'
+    sequence pieces); returns the head layout as a [P*B, S, H/P, D] tensor
+    (rank j's part is rows [j*B, (j+1)*B) of dim 0). to_heads=False: the
+    inverse; src is [P*B, S, H/P, D] and the result [B, S, H, D]."""
+    if not src.is_cuda or not src.is_contiguous() or src.dim() != 4:
+        raise ValueError("src must be a contiguous 4-d CUDA tensor")
+    if src.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("src must be bf16 or fp32")
+    if to_heads:
+        B, S, H, D = src.shape
+        if H % P:
+            raise ValueError("P must divide H")
+        shape = (P * B, S, H // P, D)
+    else:
+        PB, S, Hp, D = src.shape
+        if PB % P:
+            raise ValueError("dim 0 of a head-layout tensor is P*B")
+        B, H = PB // P, Hp * P
+        shape = (B, S, H, D)
+    if out is None:
+        out = torch.empty(shape, dtype=src.dtype, device=src.device)
+    elif tuple(out.shape) != shape or out.dtype != src.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous {shape} tensor of src's dtype")
+    _check("lcb_ulysses_all_to_all", load().lcb_ulysses_all_to_all(
+        _ptr(src), _ptr(out), B, S, H, D, P, src.element_size(),
+        ULYSSES_SEQ_TO_HEAD if to_heads else ULYSSES_HEAD_TO_SEQ, _stream(src)))
+    return out
 
 
 def cast_f32_bf16(src, dst):

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
-SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "lse_merge.cu", "noalloc.cu", "rope.cu", "cross_entropy.cu"]
+SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "lse_merge.cu", "noalloc.cu", "rope.cu", "cross_entropy.cu", "ulysses.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-strict-aliasing",
          "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]

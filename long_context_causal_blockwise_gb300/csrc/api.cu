@@ -663,6 +663,27 @@ int lcb_scatter_rows(const void* src, void* dst, const int* perm, int rows, long
   return permute_common(src, dst, perm, rows, row_bytes, 1, stream);
 }
 
+int lcb_ulysses_all_to_all(const void* src, void* dst, int B, int S, int H, int D, int P, int elem_bytes,
+                           int direction, void* stream) {
+  if (B < 1 || H < 1 || S < 0 || D < 1 || P < 1) return LCB_ERR_ARG;
+  if (H % P != 0 || S % P != 0) return LCB_ERR_ARG;
+  if (elem_bytes != 2 && elem_bytes != 4) return LCB_ERR_UNSUPPORTED;
+  if (direction != LCB_ULYSSES_SEQ_TO_HEAD && direction != LCB_ULYSSES_HEAD_TO_SEQ) return LCB_ERR_ARG;
+  const long long block_bytes = static_cast<long long>(H / P) * D * elem_bytes;
+  if (block_bytes % 16 != 0) return LCB_ERR_ARG;
+  if (S == 0) return LCB_OK;
+  if (!src || !dst || src == dst || !aligned16(src) || !aligned16(dst)) return LCB_ERR_ARG;
+  const long long rows = static_cast<long long>(B) * S;
+  const long long bv = block_bytes / 16;
+  const long long total = rows * bv * P;  // vectors in the tensor
+  const char* s0 = static_cast<const char*>(src);
+  const char* d0 = static_cast<const char*>(dst);
+  if (s0 < d0 + total * 16 && d0 < s0 + total * 16) return LCB_ERR_ARG;  // overlapping buffers
+  if (rows * bv >= (1LL << 31)) return LCB_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return finish(launch_ulysses_a2a(src, dst, rows, bv, P, direction, st), st);
+}
+
 int lcb_cast_f32_bf16(const float* src, void* dst, long long n, void* stream) {
   if (n < 0) return LCB_ERR_ARG;
   if (n == 0) return LCB_OK;

@@ -472,12 +472,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ds_tile = smem + kKvSmDs;
     const int j = kt * kT + row;
     const float c = p.scale_log2;
-    // Lane l holds LSE2/Delta of query 32x + l of a tile (loaded a tile ahead);
-    // every thread reads all 32 through warp shuffles.
+    // Lane l holds the statistics of query 32x + l of a tile (loaded a tile
+    // ahead): -LSE * log2(e) (-inf for a hidden or empty row) and
+    // -scale * Delta; every thread reads all 32 through warp shuffles. The
+    // arithmetic is the one-pass kernel's, so dK and dV match it bit for bit.
     auto load_stats = [&](int i, float& l2v, float& dlv) {
       const int q = (i0 + i) * kT + 32 * x + lane;
-      l2v = lse2_of(p, b, h, q);
-      dlv = (q < p.Sq) ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + q) : 0.f;
+      l2v = -lse2_of(p, b, h, q);
+      dlv = (q < p.Sq) ? -p.scale * __ldg(p.delta + b * p.l_bs + h * p.l_hs + q) : 0.f;
     };
     float nl2 = 0.f, ndl = 0.f;
     if (n > 0) load_stats(0, nl2, ndl);
@@ -501,11 +503,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       float pv[32];
       uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float l2 = __shfl_sync(0xffffffffu, l2v, e);
-        float pe = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2));
-        if (diag && qx + e < j) pe = 0.f;
-        pv[e] = pe;
+      for (int e = 0; e < 32; e += 2) {
+        const float m0 = __shfl_sync(0xffffffffu, l2v, e);
+        const float m1 = __shfl_sync(0xffffffffu, l2v, e + 1);
+        float x0, x1;
+        ffma2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), c, c, m0, m1);
+        pv[e] = ex2_approx(x0);
+        pv[e + 1] = ex2_approx(x1);
+      }
+      if (diag) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (qx + e < j) pv[e] = 0.f;
       }
 #pragma unroll
       for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(pv[e], pv[e + 1]);
@@ -513,13 +522,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->pt_full);  // dV(i) and S^T(i+1) may go
-      // Phase 2: dS^T = P^T (dP^T - Delta), into shared memory for dK.
+      // Phase 2: dS'^T = P^T (scale dP^T - scale Delta), into shared memory for dK.
       uint32_t dk[16];
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
         const float d0 = __shfl_sync(0xffffffffu, dlv, e);
         const float d1 = __shfl_sync(0xffffffffu, dlv, e + 1);
-        dk[e >> 1] = pack_bf16x2(pv[e] * (__uint_as_float(dp[e]) - d0), pv[e + 1] * (__uint_as_float(dp[e + 1]) - d1));
+        float t0, t1, u0, u1;
+        ffma2(t0, t1, __uint_as_float(dp[e]), __uint_as_float(dp[e + 1]), p.scale, p.scale, d0, d1);
+        fmul2(u0, u1, pv[e], pv[e + 1], t0, t1);
+        dk[e >> 1] = pack_bf16x2(u0, u1);
       }
       if (i > 0) {
         ok = warp_all(mbar_wait(&bars->ds_free, ph ^ 1u, abort_flag, p.st, kWhere | (9u << 16)));
@@ -534,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = x & 1;
     const long long off = b * p.g_bs + static_cast<long long>(j) * p.g_rs + h * kD + 64 * half;
     void* gdst = x < 2 ? p.g1 : p.g0;
-    const float mul = x < 2 ? 1.f : p.scale;
+    const float mul = 1.f;  // dK is already scaled through dS'
     const uint32_t tacc = (x < 2 ? tDV : tDK) + lane_off + 64 * half;
     if (n == 0) {
       if (valid) store_zero(gdst, off, 64, p.grad_mode);
@@ -787,24 +799,31 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     const int j = kt * kT + row;
     const bool key_ok = j < Sk;  // rows past the block's keys (zero-filled or another block's): P must be 0
     const float c = p.scale_log2;
-    auto load_stats = [&](int i, float& l2v, float& dlv) {
+    // Lane l holds the statistics of query 32x + l of a tile (loaded a tile
+    // ahead): nl2 = -LSE * log2(e) (-inf for a hidden or empty row: P = 0) and
+    // nsd = -scale * Delta. Every thread reads all 32 through warp shuffles.
+    auto load_stats = [&](int i, float& nl2v, float& nsdv) {
       const int q = (i0 + i) * kT + 32 * x + lane;
       const long long si = b * p.l_bs + h * p.l_hs + q_off + q;
       const float l = q < Sq ? __ldg(p.lse + si) : -INFINITY;
-      l2v = (l == -INFINITY) ? INFINITY : l * kLog2e;  // hidden or empty rows: P = 0
-      dlv = (q < Sq) ? __ldg(p.delta + si) : 0.f;
+      nl2v = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+      nsdv = (q < Sq) ? -p.scale * __ldg(p.delta + si) : 0.f;
     };
-    float nl2 = 0.f, ndl = 0.f;
-    if (n > 0) load_stats(0, nl2, ndl);
+    float nl2 = 0.f, nsd = 0.f;
+    if (n > 0) load_stats(0, nl2, nsd);
     bool ok = true;
     // Step s runs phase 2 of query tile s-1, phase 1 of tile s, then phase 3
     // of tile s-1: P^T(s) is computed while the tensor pipe runs dQ(s-1) and
     // dK(s-1), so the next dV and S^T can be issued as soon as dP^T(s) is.
+    // dS carries the softmax scale (dS' = scale * P (dP - Delta)), so dQ and
+    // dK come out of the MMAs scaled and are stored without a multiply.
+    // Pairs of values go through the packed f32x2 instructions.
     float pv[32];      // P^T of the tile between its phases 1 and 2
-    float dl2 = 0.f;   // Delta of that tile
+    float sd = 0.f;    // -scale * Delta of that tile
+    const float scl = p.scale;
     for (int s = 0; s <= n && ok; ++s) {
       if (s > 0) {
-        // Phase 2: dS^T = P^T (dP^T - Delta), into shared memory for dK and dQ.
+        // Phase 2: dS'^T = P^T (scale dP^T - scale Delta), into shared memory for dK and dQ.
         const int i = s - 1;
         const uint32_t ph = static_cast<uint32_t>(i) & 1u;
         ok = warp_all(mbar_wait(&bars->dp_full, ph, abort_flag, p.st, kWhere | (6u << 16)));
@@ -816,10 +835,12 @@ __global__ void __launch_bounds__(kFuThreads, 1)
           tmem_ld_x32(tDP + lane_off + 32 * x, dp);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float d0 = __shfl_sync(0xffffffffu, dl2, e);
-            const float d1 = __shfl_sync(0xffffffffu, dl2, e + 1);
-            dk[e >> 1] =
-                pack_bf16x2(pv[e] * (__uint_as_float(dp[e]) - d0), pv[e + 1] * (__uint_as_float(dp[e + 1]) - d1));
+            const float d0 = __shfl_sync(0xffffffffu, sd, e);
+            const float d1 = __shfl_sync(0xffffffffu, sd, e + 1);
+            float t0, t1, u0, u1;
+            ffma2(t0, t1, __uint_as_float(dp[e]), __uint_as_float(dp[e + 1]), scl, scl, d0, d1);
+            fmul2(u0, u1, pv[e], pv[e + 1], t0, t1);
+            dk[e >> 1] = pack_bf16x2(u0, u1);
           }
         }
         if (i > 0) {
@@ -836,21 +857,30 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         const int it = i0 + s;            // query tile
         const int qx = it * kT + 32 * x;  // first query of this warpgroup's columns
         const float l2v = nl2;
-        dl2 = ndl;
-        if (s + 1 < n) load_stats(s + 1, nl2, ndl);
+        sd = nsd;
+        if (s + 1 < n) load_stats(s + 1, nl2, nsd);
         ok = warp_all(mbar_wait(&bars->s_full, static_cast<uint32_t>(s) & 1u, abort_flag, p.st, kWhere | (5u << 16)));
         if (!ok) break;
         tc_fence_after();
-        const bool diag = causal && (it == kt);
+        // Only the diagonal tile and a ragged last key tile need a per-element mask.
+        const bool masked = __any_sync(0xffffffffu, (causal && it == kt) || !key_ok);
         {
           uint32_t sv[32];
           tmem_ld_x32(tS + lane_off + 32 * x, sv);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float l2 = __shfl_sync(0xffffffffu, l2v, e);
-            float pe = ex2_approx(fmaf(__uint_as_float(sv[e]), c, -l2));
-            if ((diag && qx + e < j) || !key_ok) pe = 0.f;
-            pv[e] = pe;
+          for (int e = 0; e < 32; e += 2) {
+            const float m0 = __shfl_sync(0xffffffffu, l2v, e);
+            const float m1 = __shfl_sync(0xffffffffu, l2v, e + 1);
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), c, c, m0, m1);
+            pv[e] = ex2_approx(x0);
+            pv[e + 1] = ex2_approx(x1);
+          }
+          if (masked) {
+            const bool diag = causal && (it == kt);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if ((diag && qx + e < j) || !key_ok) pv[e] = 0.f;
           }
         }
         {
@@ -884,21 +914,19 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         }
         if (!ok) break;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          *reinterpret_cast<float4*>(stg_row + ((ch ^ (row & 7)) << 4)) =
-              make_float4(__uint_as_float(g[4 * ch]) * p.scale, __uint_as_float(g[4 * ch + 1]) * p.scale,
-                          __uint_as_float(g[4 * ch + 2]) * p.scale, __uint_as_float(g[4 * ch + 3]) * p.scale);
-        }
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4*>(stg_row + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(g[4 * ch], g[4 * ch + 1], g[4 * ch + 2], g[4 * ch + 3]);
         fence_proxy_async_smem();
         mbar_arrive(&bars->stg_full[x]);
       }
     }
-    // Epilogue: warpgroups 0/1 write dV columns [0,64)/[64,128), 2/3 write dK (scaled).
+    // Epilogue: warpgroups 0/1 write dV columns [0,64)/[64,128), 2/3 write dK (already scaled through dS').
     const bool valid = j < Sk;
     const int half = x & 1;
     const long long off = b * p.g_bs + static_cast<long long>(k_off + j) * p.g_rs + h * kD + 64 * half;
     void* gdst = x < 2 ? p.g1 : p.g0;
-    const float mul = x < 2 ? 1.f : p.scale;
+    const float mul = 1.f;
     const uint32_t tacc = (x < 2 ? tDV : tDK) + lane_off + 64 * half;
     if (n == 0) {
       if (valid) store_zero(gdst, off, 64, p.grad_mode);
@@ -1037,8 +1065,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ds_tile = smem + kQSmDs;
     const int qi = qt * kT + row;
     const float c = p.scale_log2;
-    const float l2 = lse2_of(p, b, h, qi);
-    const float dl = (qi < p.Sq) ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + qi) : 0.f;
+    const float nl2 = -lse2_of(p, b, h, qi);
+    const float nsd = (qi < p.Sq) ? -p.scale * __ldg(p.delta + b * p.l_bs + h * p.l_hs + qi) : 0.f;
     const int q_first = qt * kT;
     const int lim = p.causal ? std::min(qi + 1, p.Sk) : p.Sk;  // keys < lim are visible
     bool ok = true;
@@ -1053,16 +1081,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars->s_free);  // S(j), dP(j) are in registers: their TMEM may take S(j+1), dP(j+1)
       const int kbase = j * kT + 32 * x;
       const bool need_mask = (p.causal && kbase + 31 > q_first) || (kbase + 32 > p.Sk);
+      // dS' = P (scale dP - scale Delta): dQ comes out of the MMA scaled
       uint32_t ds[16];
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
-        float p0 = ex2_approx(fmaf(__uint_as_float(s[e]), c, -l2));
-        float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -l2));
+        float x0, x1, t0, t1, u0, u1;
+        ffma2(x0, x1, __uint_as_float(s[e]), __uint_as_float(s[e + 1]), c, c, nl2, nl2);
+        float p0 = ex2_approx(x0);
+        float p1 = ex2_approx(x1);
         if (need_mask) {
           if (kbase + e >= lim) p0 = 0.f;
           if (kbase + e + 1 >= lim) p1 = 0.f;
         }
-        ds[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - dl), p1 * (__uint_as_float(dp[e + 1]) - dl));
+        ffma2(t0, t1, __uint_as_float(dp[e]), __uint_as_float(dp[e + 1]), p.scale, p.scale, nsd, nsd);
+        fmul2(u0, u1, p0, p1, t0, t1);
+        ds[e >> 1] = pack_bf16x2(u0, u1);
       }
       if (j > 0) {
         ok = warp_all(mbar_wait(&bars->ds_free, ph ^ 1u, abort_flag, p.st, kWhere | (9u << 16)));
@@ -1083,7 +1116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t a[32];
         tmem_ld_x32(tDQ + lane_off + x * 32, a);
-        if (valid) store_grad_chunk(p.g0, off, a, p.scale, p.grad_mode);
+        if (valid) store_grad_chunk(p.g0, off, a, 1.f, p.grad_mode);  // scaled through dS'
       }
     }
   }

@@ -308,9 +308,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < 128; ++cc)
           if (kbase + cc >= lim) s[cc] = __float_as_uint(-INFINITY);
       }
-      float mx = __uint_as_float(s[0]);
+      // Row maximum: four chains of three-input maxima (64 instructions for 128 values).
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int cc = 1; cc < 128; ++cc) mx = fmaxf(mx, __uint_as_float(s[cc]));
+      for (int cc = 0; cc < 128; cc += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          m4[k] = fmax3(m4[k], __uint_as_float(s[cc + 2 * k]), __uint_as_float(s[cc + 2 * k + 1]));
+      const float mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
       const float m_new = fmaxf(m, mx * c);
       if (j == 0) {
         m = m_new;
@@ -333,17 +338,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float sum0 = 0.f, sum1 = 0.f;
+      // p = 2^(c s - m) for pairs of values (packed f32x2 FMA and sums).
+      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * i]), c, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), c, neg_m));
-        sum0 += p0;
-        sum1 += p1;
+        float x0, x1;
+        ffma2(x0, x1, __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]), c, c, neg_m, neg_m);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        if (i & 1)
+          fadd2(sb0, sb1, sb0, sb1, p0, p1);
+        else
+          fadd2(sa0, sa1, sa0, sa1, p0, p1);
         pk[i] = pack_bf16x2(p0, p1);
       }
-      l += sum0 + sum1;
+      l += (sa0 + sb0) + (sa1 + sb1);
       tmem_st_x64(tS, pk);
       tc_fence_before();
       mbar_arrive(&bars->p_full[t]);

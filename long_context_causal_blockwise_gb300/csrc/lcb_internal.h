@@ -105,6 +105,11 @@ int launch_fill_empty(void* o, int o_f32, long long o_row_stride, long long o_ba
 
 int launch_wait_selftest(DevStatus st, cudaStream_t stream);
 
+// Ulysses all-to-all over 16-byte vectors: rows = B * S rows of P blocks of bv
+// vectors; dir 0 sequence -> head layout, 1 head -> sequence layout.
+int launch_ulysses_a2a(const void* src, void* dst, long long rows, long long bv, int P, int dir,
+                       cudaStream_t stream);
+
 int launch_cast_f32_bf16(const float* src, void* dst, long long n, cudaStream_t stream);
 
 // Cross-entropy over rows of bf16 logits streamed through registers (mode LCB_CE_*).

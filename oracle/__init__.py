@@ -23,6 +23,8 @@ Sources (the web pages on EasyContext, cited by title and section):
     (prepare_seq_parallel_inputs).
   * "EasyContext核心技术解析…", §1 "序列并行技术": ring attention, whose ring
     steps compose by merging partial results over disjoint key sets.
+  * "EasyContext核心技术解析…", §1 "序列并行技术": Ulysses attention, the
+    sequence <-> head all-to-all around per-head attention (ulysses.py).
   * "EasyContext核心技术解析…", §3 "RoPE扩展技术": the raised rotary base
     (rope.py).
   * "EasyContext内存优化秘籍DeepSpeed Zero3卸载策略详解", §进阶优化与其他技术结合:
@@ -44,4 +46,6 @@ from .attention import (  # noqa: F401
 from .merge import lse_merge  # noqa: F401
 from .rope import rope  # noqa: F401
 from .cross_entropy import ce_fwd, ce_grad, ce_lse  # noqa: F401
+from .ulysses import seq_to_head as ulysses_seq_to_head, head_to_seq as ulysses_head_to_seq  # noqa: F401
+from .ulysses import ulysses_attn_fwd  # noqa: F401
 from .zigzag import zigzag_schedule, zigzag_tasks_pairs, TASK_DIAG, TASK_LOWER, TASK_UPPER  # noqa: F401

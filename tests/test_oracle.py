@@ -619,3 +619,66 @@ def test_planted_ce_mistakes_are_caught():
     assert not np.allclose(p, oracle.ce_grad(x, y, 1.0), atol=1e-3)
     loss, lse = oracle.ce_fwd(x, y)
     assert not np.allclose(x[[0, 1], y] - lse, loss, atol=1e-3)
+
+
+# ---------------------------------------------------------------- Ulysses all-to-all
+
+def test_ulysses_golden_s4_h4_p2():
+    """Where every (row, head) lands after the all-to-all, derived by hand."""
+    g = _read_golden("ulysses_s4_h4_p2.txt")
+    S, H, P, n = 4, 4, 2, 2
+    x = np.zeros((1, S, H, 1))
+    for s in range(S):
+        for h in range(H):
+            x[0, s, h, 0] = 10 * s + h  # a distinct tag per (row, head)
+    parts = oracle.ulysses_seq_to_head(x, P)
+    assert len(g["map"]) == P * S * (H // P)
+    for j, s, hh, r, sl, h in ([int(t) for t in toks] for toks in g["map"]):
+        assert s == r * n + sl  # the row came from rank r's piece
+        assert parts[j][0, s, hh, 0] == 10 * s + h
+
+
+@pytest.mark.parametrize("B,S,H,D,P", [(1, 8, 4, 3, 2), (2, 12, 6, 2, 3), (1, 16, 8, 4, 8), (2, 6, 5, 2, 1)])
+def test_ulysses_round_trip_and_block_sizes(B, S, H, D, P):
+    rng = np.random.default_rng(S * H + P)
+    x = rng.standard_normal((B, S, H, D))
+    parts = oracle.ulysses_seq_to_head(x, P)
+    assert all(p.shape == (B, S, H // P, D) for p in parts)
+    # rank j holds all rows of head group j and nothing else
+    for j, p in enumerate(parts):
+        assert np.array_equal(p, x[:, :, j * (H // P):(j + 1) * (H // P)])
+    assert np.array_equal(oracle.ulysses_head_to_seq(parts, P), x)
+    bad = np.zeros((1, S + 1, H, D)) if P > 1 else np.zeros((1, S, H, D))
+    with pytest.raises(ValueError):  # a sequence P does not divide, or no ranks
+        oracle.ulysses_seq_to_head(bad, P if P > 1 else 0)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_ulysses_attention_equals_monolithic(causal):
+    rng = np.random.default_rng(7)
+    B, S, H, D, P = 2, 12, 6, 4, 3
+    q, k, v = (rng.standard_normal((B, S, H, D)) for _ in range(3))
+    o, lse = oracle.ulysses_attn_fwd(q, k, v, P, causal, 0.5)
+    om, lsem = oracle.attn_fwd(q, k, v, causal, 0.5)
+    np.testing.assert_allclose(o, om, atol=1e-13)
+    np.testing.assert_allclose(lse, lsem, atol=1e-13)
+
+
+def test_ulysses_pins_catch_a_transposed_exchange(monkeypatch):
+    """A planted mistake: the receiving rank takes head group r (the sender's
+    index) instead of its own j. The golden map must fail."""
+    import oracle.ulysses as oul
+
+    def wrong(x, P):
+        B, S, H, D = x.shape
+        n, hp = S // P, H // P
+        out = [np.empty((B, S, hp, D)) for _ in range(P)]
+        for r in range(P):
+            for j in range(P):
+                out[j][:, r * n:(r + 1) * n] = x[:, r * n:(r + 1) * n, r * hp:(r + 1) * hp]
+        return out
+
+    monkeypatch.setattr(oracle, "ulysses_seq_to_head", wrong)
+    monkeypatch.setattr(oul, "seq_to_head", wrong)
+    with pytest.raises(AssertionError):
+        test_ulysses_golden_s4_h4_p2()
