@@ -712,6 +712,20 @@ def run_zigzag(args):
     return 0 if bits == 0 else 3
 
 
+def run_ulysses(args):
+    """Times Ulysses over P = 8 emulated ranks (all-to-all kernel and fwd+bwd
+    against monolithic attention); prints one JSON line (not the headline)."""
+    import long_context_causal_blockwise_gb300 as lcb
+
+    lcb.load()
+    rec = ulysses_record(max(3, args.warmup), max(1, min(args.steps, 5)), 0)
+    rec["metric"] = "Ulysses all-to-all + attention, P=8 emulated ranks, B1 H32 S131072 D128"
+    bits, _ = lcb.take_device_status()
+    rec["device_status"] = bits
+    print(json.dumps(rec), flush=True)
+    return 0 if bits == 0 else 3
+
+
 def run_rope(args):
     """Times the RoPE kernel (theta = 1e6) on one [1, S, H, 128] bf16 tensor at
     the long-context stress size S = 524288, H = 32 (4.3 GB), in place, and
@@ -822,6 +836,8 @@ def main():
                     help="time the RoPE kernel on a [1, 524288, 32, 128] tensor")
     ap.add_argument("--zigzag", action="store_true",
                     help="time the one-device zigzag ring (S=131072, P=8) against monolithic attention")
+    ap.add_argument("--ulysses", action="store_true",
+                    help="time Ulysses over P=8 emulated ranks (S=131072, H=32) against monolithic attention")
     ap.add_argument("--print-kernel-hashes", action="store_true",
                     help="print the source hash of each kernel (for recording ncu traffic) and exit")
     args = ap.parse_args()
@@ -829,6 +845,8 @@ def main():
         return run_zigzag(args)
     if args.rope:
         return run_rope(args)
+    if args.ulysses:
+        return run_ulysses(args)
     if args.ce:
         return run_ce(args)
     if args.print_kernel_hashes:
