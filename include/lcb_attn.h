@@ -209,15 +209,18 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const float* lse, c
  * attn_bwd_fused_ex — attn_bwd_ex's gradients in ONE pass over the (key tile,
  * query tile) pairs, [FA] §2: each CTA owns 128 keys, keeps dK and dV in
  * TMEM, and adds every query tile's partial dQ = scale * dS K into a TILED
- * fp32 accumulator with bulk asynchronous reductions. Five tensor-core
- * products per tile pair instead of the two passes' seven (dQ's S and dP are
- * not recomputed). dQ's summation order is not fixed.
+ * fp32 accumulator by reductions in L2 (bulk asynchronous reductions for
+ * columns 0-63, vector reductions for 64-127). Five tensor-core products per
+ * tile pair instead of the two passes' seven (dQ's S and dP are not
+ * recomputed). dQ's summation order is not fixed.
  * dq_tiles: fp32, the tile holding this call's query rows [128t, 128t+128) of
  *   (b, h) starts at dq_tiles + b*dq_tile_batch_stride + h*dq_tile_head_stride
  *   + t*16384 (floats; 16-byte aligned; strides multiples of 4). Inside a
- *   tile, block x = 0..3 (columns [32x, 32x+32)) is at x*4096, row r of the
- *   block at r*32, and its four-float chunk c (columns 32x+4c..) at chunk
- *   position c ^ (r & 7). ALWAYS added into: zero it for a fresh gradient;
+ *   tile, columns 0-63 are two blocks: block x = 0, 1 (columns [32x, 32x+32))
+ *   at x*4096, row r of the block at r*32, and its four-float chunk c
+ *   (columns 32x+4c..) at chunk position c ^ (r & 7); columns 64-127 are
+ *   chunk-major: the four floats of chunk c (columns 64+4c..64+4c+3) of row r
+ *   at 8192 + (c*128 + r)*4. ALWAYS added into: zero it for a fresh gradient;
  *   lcb_dq_untile converts it to bf16 rows. A ring whose query blocks start
  *   at multiples of 128 rows accumulates all its steps into one such buffer.
  * grad_mode applies to dk and dv only (LCB_GRAD_BF16: bf16 overwritten;

@@ -10,8 +10,10 @@
 // Two forms:
 //   one pass (attn_bwd's): one CTA per 128-key tile, looping over 128-query
 //     tiles, forming dK, dV and every query tile's dQ partial; the partials
-//     are added into a tiled fp32 accumulator by bulk asynchronous reductions
-//     (five MMAs per tile pair; dQ's summation order is not fixed);
+//     are added into a tiled fp32 accumulator in L2, half by bulk
+//     asynchronous reductions from shared memory, half by vector reductions
+//     from registers (five MMAs per tile pair; dQ's summation order is not
+//     fixed);
 //   two passes, each deterministic (no reductions across CTAs):
 //     dK/dV pass: one CTA per 128-key tile, looping over 128-query tiles;
 //     dQ pass:    one CTA per 128-query tile, looping over 128-key tiles
@@ -68,8 +70,8 @@ struct Bars {
   uint64_t acc_full;
   uint64_t dq_full;   // fused pass: the dQ partial of one query tile is in TMEM
   uint64_t dq_free;   // fused pass: it was loaded by every compute thread
-  uint64_t stg_full[4];  // fused pass: warpgroup x's dQ block is staged
-  uint64_t stg_free[4];  // fused pass: warpgroup x's staged block was read by the reducer
+  uint64_t stg_full[2];  // fused pass: warpgroup x's (x = 0, 1) dQ block is staged
+  uint64_t stg_free[2];  // fused pass: warpgroup x's staged block was read by the reducer
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -572,23 +574,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 // MN-major from the dS^T tile, B = K read MN-major). Five MMAs per pair
 // instead of the seven of the two passes (dQ's S and dP are not recomputed).
 // The 128 x 128 fp32 partial of each pair is added into a tiled fp32 dQ
-// accumulator by bulk asynchronous reductions (whole 16 KB blocks, full
-// cache lines), not by per-thread atomics; its summation order is not fixed.
+// accumulator in L2; its summation order is not fixed. Two paths share the
+// work, because each alone stalls: warpgroups 0 and 1 stage their 128 x 32
+// blocks (columns 0-63) in a shared-memory slot each, which the reducer warp
+// adds with one bulk asynchronous reduction per block; warpgroups 2 and 3 add
+// columns 64-127 straight from registers with red.global.add.v4.f32, each
+// warp instruction covering 512 contiguous bytes. With all four blocks staged
+// through two slots, warpgroups 2 and 3 waited about 1500 clocks per tile for
+// the bulk engine to finish reading warpgroups 0 and 1's blocks; with all four
+// blocks as register reductions, L2 took longer to absorb them.
 //
 // Accumulator layout (floats): the tile of query rows [128t, 128t + 128) of
-// (b, h) is at dq + b * tile_bs + h * tile_hs + t * 16384, made of 4 blocks of
-// 4096 (columns [32x, 32x + 32)); row r of block x holds its 8 four-float
-// chunks c at chunk position c ^ (r & 7) (128 B per row).
+// (b, h) is at dq + b * tile_bs + h * tile_hs + t * 16384. Columns 0-63 are
+// two blocks of 4096 (block x = columns [32x, 32x + 32) at x * 4096): row r
+// of block x holds its 8 four-float chunks c at chunk position c ^ (r & 7)
+// (128 B per row). Columns 64-127 are chunk-major from float 8192 on: the
+// four floats of chunk c (columns 64 + 4c .. 64 + 4c + 3) of row r at
+// 8192 + (c * 128 + r) * 4.
 //
 // TMEM as in the dK/dV pass; the dQ partial of query tile i reuses the dP^T
 // columns once dP^T(i) is in registers. Shared memory: K, V, a 2-slot Q ring,
 // ONE dO slot (dO(i+1) loads while dS(i) is formed), dS^T, and two 16 KB
-// staging slots for dQ blocks (warpgroups x and x + 2 share slot x & 1).
+// staging slots for dQ blocks (slot x for warpgroup x = 0, 1).
 // Warps 0-15 compute, 16 TMA producer, 17 MMA issuer, 18 dQ reducer.
 // MMA order per query tile i: dV += P^T dO_i, S^T(i+1), dQ(i),
 // dK += dS^T Q_i, then dP^T(i+1) once dQ(i) has been read out. The compute
 // warps form dS^T(i), then P^T(i+1) while dQ(i) and dK(i) run, then read
-// out and stage dQ(i).
+// out dQ(i) and add it into the accumulator.
 constexpr int kFuThreads = 608;
 constexpr int kFuReduceWarp = 18;
 constexpr uint32_t kDqBlock = 128 * 32 * 4;  // one staged dQ block: 128 rows x 32 columns fp32
@@ -604,6 +616,12 @@ constexpr uint32_t kFuSmem = kFuSmBar + sizeof(Bars) + 1024;
 __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
                "r"(bytes)
+               : "memory");
+}
+// Adds four floats at gaddr (16-byte aligned) in L2, fire and forget.
+__device__ __forceinline__ void red_add_v4(float* gaddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gaddr), "f"(__uint_as_float(a)),
+               "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -644,7 +662,7 @@ __global__ void __launch_bounds__(kFuThreads, 1)
   const int n = std::max(0, nq - i0);  // query tiles
 
   if (threadIdx.x == 0) {
-    for (int x = 0; x < 4; ++x) {
+    for (int x = 0; x < 2; ++x) {
       mbar_init(&bars->stg_full[x], 128);
       mbar_init(&bars->stg_free[x], 1);
     }
@@ -762,28 +780,28 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     }
     __syncwarp();
   } else if (warp == kFuReduceWarp) {
-    // Adds each staged 16 KB dQ block into the accumulator; frees its slot once
-    // read. Blocks x and x + 1 sit in different slots, so both reductions are
-    // issued before the first read is waited for: the two reads overlap.
+    // Adds the two staged 16 KB dQ blocks of each tile (columns 0-63) into the
+    // accumulator and frees each slot once read; both reductions are issued
+    // before the first read is waited for, so the two reads overlap.
     if (lane == 0 && n > 0) {
       bool ok = true;
       for (int i = 0; i < n && ok; ++i) {
         const uint32_t ph = static_cast<uint32_t>(i) & 1u;
         float* tile =
             p.dq_acc + b * p.dq_bs + h * p.dq_hs + static_cast<long long>(q_off / kT + i0 + i) * (kT * kD);
-        for (int x = 0; x < 4 && ok; x += 2) {  // blocks 0, 1 in slots 0, 1, then 2, 3 reusing them
-          ok = mbar_wait(&bars->stg_full[x], ph, abort_flag, p.st, kWhere | (14u << 16));
+        {  // blocks 0 and 1 (columns 0-63), each in a slot of its own
+          ok = mbar_wait(&bars->stg_full[0], ph, abort_flag, p.st, kWhere | (14u << 16));
           if (!ok) break;
-          bulk_reduce_add_f32(tile + x * (kDqBlock / 4), sbase + kFuSmStg, kDqBlock);
+          bulk_reduce_add_f32(tile, sbase + kFuSmStg, kDqBlock);
           bulk_commit();
-          ok = mbar_wait(&bars->stg_full[x + 1], ph, abort_flag, p.st, kWhere | (14u << 16));
+          ok = mbar_wait(&bars->stg_full[1], ph, abort_flag, p.st, kWhere | (14u << 16));
           if (!ok) break;
-          bulk_reduce_add_f32(tile + (x + 1) * (kDqBlock / 4), sbase + kFuSmStg + kDqBlock, kDqBlock);
+          bulk_reduce_add_f32(tile + kDqBlock / 4, sbase + kFuSmStg + kDqBlock, kDqBlock);
           bulk_commit();
-          bulk_wait_read<1>();  // block x has left its slot
-          mbar_arrive(&bars->stg_free[x]);
+          bulk_wait_read<1>();
+          mbar_arrive(&bars->stg_free[0]);
           bulk_wait_read<0>();
-          mbar_arrive(&bars->stg_free[x + 1]);
+          mbar_arrive(&bars->stg_free[1]);
         }
       }
       bulk_wait_all();  // every reduction issued has completed
@@ -795,7 +813,7 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     const int row = threadIdx.x & 127;  // key row of S^T/dP^T/dV/dK, query row of dQ: the TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint8_t* ds_tile = smem + kFuSmDs;
-    uint8_t* stg_row = smem + kFuSmStg + (x & 1) * kDqBlock + row * 128;
+    uint8_t* stg_row = smem + kFuSmStg + (x & 1) * kDqBlock + row * 128;  // used by warpgroups 0 and 1
     const int j = kt * kT + row;
     const bool key_ok = j < Sk;  // rows past the block's keys (zero-filled or another block's): P must be 0
     const float c = p.scale_log2;
@@ -904,21 +922,26 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         tmem_ld_x32(tDQ + lane_off + 32 * x, g);
         tc_fence_before();
         mbar_arrive(&bars->dq_free);
-        // slot x & 1 is free once the other warpgroup's block in it was read:
-        // warpgroups 0/1 wait for 2/3's block of tile i-1, 2/3 for 0/1's block of tile i.
+        float* tile = p.dq_acc + b * p.dq_bs + h * p.dq_hs + static_cast<long long>(q_off / kT + i0 + i) * (kT * kD);
         if (x < 2) {
+          // columns [32x, 32x + 32): staged in slot x (free once its block of tile i-1 was read), bulk-reduced
           if (i > 0)
-            ok = warp_all(mbar_wait(&bars->stg_free[x + 2], ph ^ 1u, abort_flag, p.st, kWhere | (15u << 16)));
-        } else {
-          ok = warp_all(mbar_wait(&bars->stg_free[x - 2], ph, abort_flag, p.st, kWhere | (15u << 16)));
-        }
-        if (!ok) break;
+            ok = warp_all(mbar_wait(&bars->stg_free[x], ph ^ 1u, abort_flag, p.st, kWhere | (15u << 16)));
+          if (!ok) break;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(stg_row + ((ch ^ (row & 7)) << 4)) =
-              make_uint4(g[4 * ch], g[4 * ch + 1], g[4 * ch + 2], g[4 * ch + 3]);
-        fence_proxy_async_smem();
-        mbar_arrive(&bars->stg_full[x]);
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(stg_row + ((ch ^ (row & 7)) << 4)) =
+                make_uint4(g[4 * ch], g[4 * ch + 1], g[4 * ch + 2], g[4 * ch + 3]);
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->stg_full[x]);
+        } else {
+          // columns [64, 128): chunk-major half, four floats of chunk c (columns 64 + 4c..) of row r at
+          // 8192 + (c * 128 + r) * 4: one warp's reduction covers 512 contiguous bytes
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            red_add_v4(tile + 8192 + ((8 * (x - 2) + ch) * 128 + row) * 4, g[4 * ch], g[4 * ch + 1], g[4 * ch + 2],
+                       g[4 * ch + 3]);
+        }
       }
     }
     // Epilogue: warpgroups 0/1 write dV columns [0,64)/[64,128), 2/3 write dK (already scaled through dS').
@@ -961,9 +984,9 @@ __global__ void __launch_bounds__(256) dq_untile_kernel(const float* __restrict_
     const int s = static_cast<int>(bs_ % S);
     const int b = static_cast<int>(bs_ / S);
     const int r = s & (kT - 1), x = c4 >> 3, ch = c4 & 7;
-    const float4 v = __ldg(reinterpret_cast<const float4*>(acc + b * tile_bs + h * tile_hs +
-                                                           static_cast<long long>(s / kT) * (kT * kD) + x * 4096 +
-                                                           r * 32 + ((ch ^ (r & 7)) << 2)));
+    const float* tl = acc + b * tile_bs + h * tile_hs + static_cast<long long>(s / kT) * (kT * kD);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(
+        x < 2 ? tl + x * 4096 + r * 32 + ((ch ^ (r & 7)) << 2) : tl + 8192 + ((c4 - 16) * 128 + r) * 4));
     uint2 u;
     u.x = pack_bf16x2(v.x, v.y);
     u.y = pack_bf16x2(v.z, v.w);
@@ -1227,9 +1250,16 @@ __global__ void __launch_bounds__(256) dq_untile16_kernel(const float* __restric
   if (s >= S) return;
   const int k16 = threadIdx.x & 15;  // columns [8 k16, 8 k16 + 8): block k16 / 4, chunks 2 (k16 % 4) and + 1
   const int c0 = (k16 & 3) * 2;
-  const float* row = acc + b * tile_bs + h * tile_hs + static_cast<long long>(t) * (kT * kD) + (k16 >> 2) * 4096 + r * 32;
-  const float4 v0 = __ldg(reinterpret_cast<const float4*>(row + ((c0 ^ (r & 7)) << 2)));
-  const float4 v1 = __ldg(reinterpret_cast<const float4*>(row + (((c0 + 1) ^ (r & 7)) << 2)));
+  const float* tl = acc + b * tile_bs + h * tile_hs + static_cast<long long>(t) * (kT * kD);
+  float4 v0, v1;
+  if (k16 < 8) {
+    const float* row = tl + (k16 >> 2) * 4096 + r * 32;
+    v0 = __ldg(reinterpret_cast<const float4*>(row + ((c0 ^ (r & 7)) << 2)));
+    v1 = __ldg(reinterpret_cast<const float4*>(row + (((c0 + 1) ^ (r & 7)) << 2)));
+  } else {
+    v0 = __ldg(reinterpret_cast<const float4*>(tl + 8192 + ((2 * k16 - 16) * 128 + r) * 4));
+    v1 = __ldg(reinterpret_cast<const float4*>(tl + 8192 + ((2 * k16 - 15) * 128 + r) * 4));
+  }
   uint4 u;
   u.x = pack_bf16x2(v0.x, v0.y);
   u.y = pack_bf16x2(v0.z, v0.w);

@@ -150,17 +150,19 @@ def _stats(q, k, v, do, causal, scale):
 
 
 def untile_f32(tiles, S):
-    """The fused pass's tiled dQ accumulator as fp32 [B, S, H, D], undoing the
-    documented layout (block x = columns [32x, 32x+32), row r, four-float
-    chunk c at position c ^ (r & 7))."""
+    """The tiled dQ accumulator as fp32 [B, S, H, D]: columns 0-63 as two
+    row-swizzled blocks, columns 64-127 chunk-major."""
     B, H, T, _ = tiles.shape
-    t = tiles.view(B, H, T, 4, 128, 8, 4)
+    t = tiles.view(B, H, T, 16384)
+    lo = t[..., :8192].reshape(B, H, T, 2, 128, 8, 4)
     r = torch.arange(128, device=tiles.device)
     c = torch.arange(8, device=tiles.device)
-    pos = c[None, :] ^ (r[:, None] & 7)  # [128, 8]: stored position of chunk c in row r
-    g = t[:, :, :, :, r[:, None], pos, :]  # [B, H, T, 4, 128, 8, 4]
-    out = g.permute(0, 2, 4, 1, 3, 5, 6).reshape(B, T * 128, H, D)
-    return out[:, :S]
+    pos = c[None, :] ^ (r[:, None] & 7)
+    g = lo[:, :, :, :, r[:, None], pos, :]  # [B, H, T, 2, 128, 8, 4]
+    lo_rows = g.permute(0, 2, 4, 1, 3, 5, 6).reshape(B, T * 128, H, 64)
+    hi = t[..., 8192:].reshape(B, H, T, 16, 128, 4)
+    hi_rows = hi.permute(0, 2, 4, 1, 3, 5).reshape(B, T * 128, H, 64)
+    return torch.cat([lo_rows, hi_rows], dim=3)[:, :S]
 
 
 @pytest.mark.parametrize("B,H,Sq,Sk,causal", [(2, 3, 700, 700, True), (1, 2, 300, 520, False),
