@@ -411,6 +411,7 @@ def run_ours(args, rank, world, local_rank):
                  for h_, s_, theta in ((32, 131072, None), (40, 262144, None), (32, 524288, 1e6))]
         ring = zigzag_record(args.warmup, args.size_steps, local_rank)
         uly = ulysses_record(args.warmup, args.size_steps, local_rank)
+        ring["rank_balance"] = ring_balance_record(local_rank)
         sclocks = sampler.stop()
         for rec in sizes:
             pk, kind_ = tensor_peak(peaks, rec["timed_s"], sclocks)
@@ -642,6 +643,51 @@ def zigzag_record(warmup, steps, local_rank, detail=False):
     return rec
 
 
+def ring_balance_record(local_rank):
+    """The rank-local ring driver at B1 H32 S131072 over P = 8 ranks, run
+    through the one-process loopback, for the zigzag and the plain
+    (contiguous) schedule: every rank's kernel time per ring step (CUDA
+    events around its steps), the lockstep critical path (the slowest rank at
+    each step, as the ranks of a real ring wait for each other) against a
+    perfectly balanced one (total / P)."""
+    import torch
+
+    from long_context_causal_blockwise_gb300.inputs import gaussian_qkvdo
+    from long_context_causal_blockwise_gb300.ring import LoopbackRing, RingRank
+    import long_context_causal_blockwise_gb300 as lcb
+
+    Hr, Sr, Pr = 32, 131072, 8
+    dev = torch.device("cuda", local_rank)
+    q, k, v, do = gaussian_qkvdo(1, Hr, Sr, D, seed=0, device=dev)
+    out = {"workload": "rank-local ring driver, loopback of P=8 ranks on one GPU, B1 H32 S131072 D128 causal, "
+                       "fwd+bwd; transfers are device copies between the ranks' kernels"}
+    for sched in ("zigzag", "contiguous"):
+        if sched == "zigzag":
+            plan = lcb.zigzag.ZigzagPlan(Sr, Pr, dev)
+            src = [plan.gather(x) for x in (q, k, v, do)]
+        else:
+            src = [q, k, v, do]
+        n = Sr // Pr
+        mine = [[x[:, r * n:(r + 1) * n].contiguous() for x in src] for r in range(Pr)]
+        del src
+        for warm in (True, False):
+            hub = LoopbackRing(Pr, time_ranks=not warm)
+            ranks = [RingRank(r, Pr, Sr, hub.transport(r), schedule=sched) for r in range(Pr)]
+            fwd = hub.run([rk.forward_steps(*mine[r][:3]) for r, rk in enumerate(ranks)])
+            hub.run([rk.backward_steps(*mine[r][:3], fwd[r][0], fwd[r][1], mine[r][3])
+                     for r, rk in enumerate(ranks)])
+            del fwd
+        torch.cuda.synchronize()
+        steps = [[a.elapsed_time(b) for a, b in evs] for evs in hub.events]
+        per_rank = [sum(x) for x in steps]
+        critical = sum(max(steps[r][j] for r in range(Pr)) for j in range(len(steps[0])))
+        out[sched] = {"rank_ms": per_rank, "critical_path_ms": critical, "balanced_ms": sum(per_rank) / Pr,
+                      "imbalance": critical / (sum(per_rank) / Pr)}
+        del mine
+        torch.cuda.empty_cache()
+    return out
+
+
 def ulysses_record(warmup, steps, local_rank):
     """Ulysses over P = 8 emulated ranks at B1 H32 S131072: the all-to-all
     kernel alone (bytes read + written per call against the HBM peak), and
@@ -705,6 +751,7 @@ def run_zigzag(args):
 
     lcb.load()
     rec = zigzag_record(args.warmup, max(1, min(args.steps, 5)), 0, detail=True)
+    rec["rank_balance"] = ring_balance_record(0)
     rec["metric"] = "zigzag ring emulation fwd+bwd (P=8, S=131072, H=32, D=128) vs monolithic"
     bits, _ = lcb.take_device_status()
     rec["device_status"] = bits

@@ -78,6 +78,8 @@ extern "C" {
 #define LCB_TASK_DIAG 0
 #define LCB_TASK_LOWER 1
 #define LCB_TASK_UPPER 2
+#define LCB_TASK_FULL 3 /* ring_schedule: all local queries x all of src's keys */
+#define LCB_TASK_NONE 4 /* ring_schedule: src's keys follow every local query; no work */
 
 /* One attention task of the zigzag ring: rank `rank` at ring step `step`
  * attends its queries [q_off, q_off+q_len) to the keys/values it holds from
@@ -312,6 +314,20 @@ int attn_lse_merge(float* o_acc, float* lse_acc, const void* o_b, const float* l
  * Either output pointer may be NULL. Returns LCB_ERR_SCHEDULE on bad S, P.
  */
 int zigzag_schedule(int S, int P, int* perm, lcb_task* tasks);
+
+/*
+ * ring_schedule — the plain (contiguous) ring that the zigzag split improves
+ * on ([SP] §1: ring attention over sequence shards). Rank r of P holds rows
+ * [r S/P, (r+1) S/P); perm (S ints, may be NULL) is the identity. tasks
+ * (P*P entries, may be NULL) at [r*P + s], as zigzag_schedule's: at step s
+ * rank r holds the keys of src = (r - s) mod P; s = 0 DIAG (causal, local x
+ * local), src < r FULL (local queries x src's keys, non-causal), src > r NONE
+ * (q_len = k_len = 0: src's keys all follow every local query). Rank r does
+ * one causal block and r full blocks: the work grows with r, which the zigzag
+ * split evens out. Host-only. LCB_ERR_SCHEDULE unless P >= 1 and S is a
+ * positive multiple of P.
+ */
+int ring_schedule(int S, int P, int* perm, lcb_task* tasks);
 
 /* lcb_cross_entropy modes. */
 #define LCB_CE_FWD 0     /* loss and LSE; logits read only */

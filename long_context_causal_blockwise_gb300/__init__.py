@@ -5,7 +5,7 @@ thin Python binding.
 Public calls (all run in this library's CUDA kernels):
   attn_fwd, attn_fwd_ex, attn_fwd_group, attn_bwd, attn_bwd_ex, attn_bwd_group, attn_bwd_preprocess, attn_bwd_noalloc,
   dq_tiles_zeros / dq_tiles_zero_ / dq_untile (the one-pass backward's tiled dQ accumulator),
-  attn_lse_merge, zigzag_schedule, permute_rows, cast_f32_bf16,
+  attn_lse_merge, zigzag_schedule, ring_schedule, permute_rows, cast_f32_bf16,
   rope (rotary position embedding with a raised base, and its inverse),
   cross_entropy (the loss head with an in-place backward),
   zigzag_attention_fwd / zigzag_attention_bwd (the one-device zigzag ring),
@@ -39,6 +39,7 @@ from ._lib import (  # noqa: F401
     dq_untile,
     load,
     permute_rows,
+    ring_schedule,
     rope,
     selftest_bounded_wait,
     set_wait_limit_ns,

@@ -26,7 +26,7 @@ LCB_OUT_F32_MERGE = 2
 LCB_GRAD_BF16 = 0
 LCB_GRAD_F32_ACCUM = 1
 LCB_GRAD_F32_STORE = 2
-TASK_DIAG, TASK_LOWER, TASK_UPPER = 0, 1, 2
+TASK_DIAG, TASK_LOWER, TASK_UPPER, TASK_FULL, TASK_NONE = 0, 1, 2, 3, 4
 
 
 class LcbTask(ctypes.Structure):
@@ -78,6 +78,7 @@ _SIGNATURES = {
     "attn_fwd_group": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _LL, _LL, _LL, _LL, _LL, _LL, _LL, _LL,
                         ctypes.POINTER(LcbFwdTask), _I, _P], _I),
     "zigzag_schedule": ([_I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(LcbTask)], _I),
+    "ring_schedule": ([_I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(LcbTask)], _I),
     "lcb_cross_entropy": ([_P, _P, _P, _P, _P, _I, _I, _LL, _I, _I, _P], _I),
     "lcb_rope": ([_P, _P, _I, _I, _I, _I, ctypes.c_double, _LL, _I, _LL, _LL, _P], _I),
     "lcb_permute_rows": ([_P, _P, _P, _I, _LL, _P], _I),
@@ -429,6 +430,14 @@ def zigzag_schedule(S, P):
     perm = (ctypes.c_int * S)()
     tasks = (LcbTask * (P * P))()
     _check("zigzag_schedule", load().zigzag_schedule(S, P, perm, tasks))
+    return list(perm), [{f: getattr(t, f) for f, _ in LcbTask._fields_} for t in tasks]
+
+
+def ring_schedule(S, P):
+    """Host call: the plain (contiguous) ring; returns (perm list[int], tasks list[dict])."""
+    perm = (ctypes.c_int * S)()
+    tasks = (LcbTask * (P * P))()
+    _check("ring_schedule", load().ring_schedule(S, P, perm, tasks))
     return list(perm), [{f: getattr(t, f) for f, _ in LcbTask._fields_} for t in tasks]
 
 

@@ -646,6 +646,45 @@ int zigzag_schedule(int S, int P, int* perm, lcb_task* tasks) {
   return LCB_OK;
 }
 
+int ring_schedule(int S, int P, int* perm, lcb_task* tasks) {
+  if (P < 1 || S < P || S % P != 0) return LCB_ERR_SCHEDULE;
+  const int n = S / P;
+  if (perm) {
+    for (int i = 0; i < S; ++i) perm[i] = i;
+  }
+  if (tasks) {
+    for (int r = 0; r < P; ++r) {
+      for (int s = 0; s < P; ++s) {
+        const int src = ((r - s) % P + P) % P;
+        lcb_task t;
+        t.rank = r;
+        t.step = s;
+        t.src = src;
+        t.q_off = r * n;
+        t.k_off = src * n;
+        if (s == 0) {
+          t.kind = LCB_TASK_DIAG;
+          t.q_len = n;
+          t.k_len = n;
+          t.causal = 1;
+        } else if (src < r) {
+          t.kind = LCB_TASK_FULL;
+          t.q_len = n;
+          t.k_len = n;
+          t.causal = 0;
+        } else {  // every key of a later rank follows every local query
+          t.kind = LCB_TASK_NONE;
+          t.q_len = 0;
+          t.k_len = 0;
+          t.causal = 0;
+        }
+        tasks[r * P + s] = t;
+      }
+    }
+  }
+  return LCB_OK;
+}
+
 static int permute_common(const void* src, void* dst, const int* perm, int rows, long long row_bytes, int scatter,
                           void* stream) {
   if (rows < 0 || row_bytes <= 0 || (row_bytes % 16)) return LCB_ERR_ARG;

@@ -7,6 +7,10 @@ same page, 技术实现细节 › 异步通信优化) with the zigzag split
 zigzag_ring_attn): rank r of P holds sequence chunks r and 2P-1-r of Q, K,
 V (its 2c rows, c = S / 2P) and never sees another rank's memory.
 
+The plain (contiguous) ring is the same driver with schedule="contiguous":
+rank r holds rows [r S/P, (r+1) S/P), and its steps that hold a later
+rank's keys compute nothing.
+
 Forward, ring step s = 0 .. P-1: the rank holds the K/V pair of rank
 src = (r - s) mod P in a local buffer. Before computing with it, it starts
 sending that pair to rank r+1 and receiving rank r-1's pair into a second
@@ -114,27 +118,37 @@ class RingCompute:
         _lib.cast_f32_bf16(dv_acc, dv)
 
 
-def rank_tasks(S, P, rank):
+def rank_tasks(S, P, rank, schedule="zigzag"):
     """Rank `rank`'s ring tasks in step order, with row offsets relative to
-    its own chunk pair (q_rel) and to the holder's chunk pair (k_rel)."""
-    _, tasks = _lib.zigzag_schedule(S, P)
-    c2 = S // P
+    its own rows (q_rel) and to the holder's rows (k_rel). schedule "zigzag"
+    (chunks r and 2P-1-r) or "contiguous" (the plain ring, rows [r S/P, (r+1)
+    S/P)); either way a rank holds S/P rows."""
+    sched = {"zigzag": _lib.zigzag_schedule, "contiguous": _lib.ring_schedule}[schedule]
+    _, tasks = sched(S, P)
+    n = S // P
     mine = sorted((t for t in tasks if t["rank"] == rank), key=lambda t: t["step"])
     for t in mine:
-        t["q_rel"] = t["q_off"] - rank * c2
-        t["k_rel"] = t["k_off"] - t["src"] * c2
+        t["q_rel"] = t["q_off"] - rank * n
+        t["k_rel"] = t["k_off"] - t["src"] * n
     return mine
 
 
 class RingRank:
-    """One rank of the zigzag ring: its own chunk pair, its tasks, a transport."""
+    """One rank of the ring: its own rows, its tasks, a transport.
 
-    def __init__(self, rank, P, S, transport, compute=None, scale=None):
-        if S % (2 * P):
+    schedule "zigzag" balances the causal work across ranks; "contiguous" is
+    the plain ring (rank r's work grows with r; its steps that hold a later
+    rank's keys have nothing to compute and only pass the keys on)."""
+
+    def __init__(self, rank, P, S, transport, compute=None, scale=None, schedule="zigzag"):
+        if schedule == "zigzag" and S % (2 * P):
             raise ValueError("the zigzag split needs S a multiple of 2P")
+        if S % P:
+            raise ValueError("the ring needs S a multiple of P")
         self.rank, self.P, self.S = rank, P, S
-        self.c = S // (2 * P)
-        self.tasks = rank_tasks(S, P, rank)
+        self.n = S // P  # rows per rank
+        self.schedule = schedule
+        self.tasks = rank_tasks(S, P, rank, schedule)
         self.transport = transport
         self.compute = RingCompute() if compute is None else compute
         self.scale = scale
@@ -145,8 +159,8 @@ class RingRank:
         resuming it), and returns (o bf16, lse fp32 [1, H, 2c], o_acc fp32) of
         this rank's rows."""
         B, n, H, D = q.shape
-        if B != 1 or n != 2 * self.c:
-            raise ValueError("a rank holds [1, 2c, H, D] of each tensor")
+        if B != 1 or n != self.n:
+            raise ValueError("a rank holds [1, S/P, H, D] of each tensor")
         scale = D ** -0.5 if self.scale is None else self.scale
         o_acc = torch.empty((1, n, H, D), dtype=torch.float32, device=q.device)
         lse = torch.empty((1, H, n), dtype=torch.float32, device=q.device)
@@ -157,7 +171,8 @@ class RingRank:
             if s + 1 < self.P:  # pass the pair on while this step computes with it
                 nxt = stage[s % 2]
                 handles.append(self.transport.exchange(list(cur), list(nxt)))
-            self.compute.fwd(task, q, cur[0], cur[1], o_acc, lse, scale)
+            if task["q_len"] and task["k_len"]:
+                self.compute.fwd(task, q, cur[0], cur[1], o_acc, lse, scale)
             yield handles
             if s + 1 < self.P:
                 cur = nxt
@@ -173,7 +188,8 @@ class RingRank:
         dev = q.device
         delta = torch.empty((1, H, n), dtype=torch.float32, device=dev)
         self.compute.delta(o, do, delta)
-        fused = fused and self.c % 128 == 0
+        # the tiled dQ accumulator takes query blocks that start on 128-row tiles
+        fused = fused and all(t["q_rel"] % 128 == 0 for t in self.tasks)
         # dQ: the one-pass backward adds into a zeroed tiled accumulator; the
         # two-pass form stores at step 0 (the DIAG task covers every local row)
         dq_acc = (_lib.dq_tiles_zeros(1, H, n, dev) if fused else
@@ -188,7 +204,8 @@ class RingRank:
             if s + 1 < self.P:  # K and V are read-only: pass them on before computing
                 nxt = kv_stage[s % 2]
                 handles.append(self.transport.exchange(list(cur), list(nxt)))
-            self.compute.bwd(task, q, cur[0], cur[1], lse, delta, do, dq_acc, acc[0], acc[1], scale)
+            if task["q_len"] and task["k_len"]:
+                self.compute.bwd(task, q, cur[0], cur[1], lse, delta, do, dq_acc, acc[0], acc[1], scale)
             # the accumulators go on with this step's contribution; the hop after
             # step P-1 brings every rank its own keys' accumulators
             nacc = acc_stage[s % 2]
@@ -226,9 +243,16 @@ class LoopbackRing:
     and after each round every posted transfer is made as a device copy on
     the current stream: after the senders' step, before the receivers' next."""
 
-    def __init__(self, P):
+    def __init__(self, P, time_ranks=False):
         self.P = P
         self.posted = [[] for _ in range(P)]
+        # optional: CUDA events around every rank's steps (its kernels only, not the transfers)
+        self.events = [[] for _ in range(P)] if time_ranks else None
+
+    def rank_ms(self):
+        """Milliseconds of kernel time per rank (time_ranks=True; synchronises)."""
+        torch.cuda.synchronize()
+        return [sum(a.elapsed_time(b) for a, b in evs) for evs in self.events]
 
     def transport(self, rank):
         hub = self
@@ -261,11 +285,17 @@ class LoopbackRing:
         while live:
             still = []
             for r in live:
+                if self.events is not None:
+                    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    ev[0].record()
                 try:
                     next(gens[r])
                     still.append(r)
                 except StopIteration as stop:
                     results[r] = stop.value
+                if self.events is not None:
+                    ev[1].record()
+                    self.events[r].append(ev)
             if still and len(still) != self.P:
                 raise RuntimeError("ranks left the ring at different steps")
             self._deliver()

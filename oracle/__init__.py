@@ -49,3 +49,4 @@ from .cross_entropy import ce_fwd, ce_grad, ce_lse  # noqa: F401
 from .ulysses import seq_to_head as ulysses_seq_to_head, head_to_seq as ulysses_head_to_seq  # noqa: F401
 from .ulysses import ulysses_attn_fwd  # noqa: F401
 from .zigzag import zigzag_schedule, zigzag_tasks_pairs, TASK_DIAG, TASK_LOWER, TASK_UPPER  # noqa: F401
+from .zigzag import ring_schedule, TASK_FULL, TASK_NONE  # noqa: F401

@@ -74,3 +74,37 @@ def zigzag_tasks_pairs(S, perm, tasks):
                     continue
                 count[perm[t["q_off"] + a], perm[t["k_off"] + b]] += 1
     return count
+
+
+TASK_FULL, TASK_NONE = 3, 4
+
+
+def ring_schedule(S, P):
+    """The plain ring: the contiguous split the zigzag split improves on.
+
+    Rank r holds rows [r S/P, (r+1) S/P) (perm is the identity). At step s it
+    holds the keys of src = (r - s) mod P:
+      s = 0, DIAG : local queries x local keys, causal;
+      src < r, FULL: all local queries x all of src's keys, all visible;
+      src > r, NONE: src's keys all follow every local query: no work.
+    Rank r does r full blocks and one causal block, so the last rank does
+    about 2(P-1)/P times the average work; the zigzag split makes every
+    rank's work equal.
+    """
+    if P < 1 or S < P or S % P != 0:
+        raise ValueError("the contiguous ring needs P >= 1 and S a positive multiple of P")
+    n = S // P
+    perm = np.arange(S, dtype=np.int64)
+    tasks = []
+    for r in range(P):
+        for s in range(P):
+            src = (r - s) % P
+            if s == 0:
+                kind, q_len, k_len, causal = TASK_DIAG, n, n, 1
+            elif src < r:
+                kind, q_len, k_len, causal = TASK_FULL, n, n, 0
+            else:
+                kind, q_len, k_len, causal = TASK_NONE, 0, 0, 0
+            tasks.append({"rank": r, "step": s, "src": src, "kind": kind, "q_off": r * n, "q_len": q_len,
+                          "k_off": src * n, "k_len": k_len, "causal": causal})
+    return perm, tasks

@@ -144,6 +144,20 @@ def test_zigzag_schedule_matches_oracle_bit_exact(lib, S, P):
     assert tasks == otasks
 
 
+@pytest.mark.parametrize("S,P", [(6, 3), (8, 1), (4096, 8), (131072, 8), (100, 5)])
+def test_ring_schedule_matches_oracle_bit_exact(lib, S, P):
+    perm, tasks = _lib.ring_schedule(S, P)
+    operm, otasks = oracle.ring_schedule(S, P)
+    assert np.array_equal(np.array(perm), operm)
+    assert tasks == otasks
+
+
+def test_ring_schedule_rejects_bad_sizes(lib):
+    nul = ctypes.POINTER(ctypes.c_int)()
+    for S, P in ((7, 2), (0, 1), (4, 0), (3, 4)):
+        assert lib.ring_schedule(S, P, nul, None) == _lib.LCB_ERR_SCHEDULE
+
+
 def test_zigzag_schedule_rejects_bad_sizes(lib):
     for S, P in ((10, 3), (0, 1), (8, 0), (3, 2), (-8, 2)):
         assert lib.zigzag_schedule(S, P, None, None) == _lib.LCB_ERR_SCHEDULE

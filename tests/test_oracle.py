@@ -682,3 +682,49 @@ def test_ulysses_pins_catch_a_transposed_exchange(monkeypatch):
     monkeypatch.setattr(oul, "seq_to_head", wrong)
     with pytest.raises(AssertionError):
         test_ulysses_golden_s4_h4_p2()
+
+
+# ---------------------------------------------------------------- plain (contiguous) ring
+
+def test_ring_golden_s6_p3():
+    g = _read_golden("ring_s6_p3.txt")
+    perm, tasks = oracle.ring_schedule(6, 3)
+    assert [int(x) for x in g["perm"][0]] == list(perm)
+    got = sorted((t["rank"], t["step"], t["src"], t["kind"], t["q_off"], t["q_len"], t["k_off"], t["k_len"],
+                  t["causal"]) for t in tasks)
+    assert got == sorted(tuple(int(x) for x in toks) for toks in g["task"])
+
+
+def _pairs_per_rank(S, perm, tasks, P):
+    per = np.zeros(P, dtype=np.int64)
+    for t in tasks:
+        one = {**t}
+        per[t["rank"]] += oracle.zigzag_tasks_pairs(S, perm, [one]).sum()
+    return per
+
+
+@pytest.mark.parametrize("P,n", [(1, 4), (2, 3), (3, 2), (4, 4), (8, 2)])
+def test_ring_covers_every_causal_pair_once_with_rank_imbalance(P, n):
+    S = P * n
+    perm, tasks = oracle.ring_schedule(S, P)
+    count = oracle.zigzag_tasks_pairs(S, perm, tasks)
+    want = np.tril(np.ones((S, S), dtype=np.int64))
+    assert np.array_equal(count, want)  # every causal pair exactly once
+    per = _pairs_per_rank(S, perm, tasks, P)
+    # rank r: one causal block and r full blocks
+    assert list(per) == [n * (n + 1) // 2 + r * n * n for r in range(P)]
+    assert per.sum() == S * (S + 1) // 2
+    # the zigzag split of the same sequence (when it exists) gives every rank the same count
+    if S % (2 * P) == 0:
+        zperm, ztasks = oracle.zigzag_schedule(S, P)
+        zper = _pairs_per_rank(S, zperm, ztasks, P)
+        assert len(set(zper.tolist())) == 1 and zper.sum() == per.sum()
+    for t in tasks:  # a NONE task has no work, and only later ranks' keys give NONE
+        if t["kind"] == oracle.TASK_NONE:
+            assert t["q_len"] == 0 and t["k_len"] == 0 and t["src"] > t["rank"]
+
+
+def test_ring_rejects_bad_sizes():
+    for S, P in ((7, 2), (0, 1), (4, 0), (3, 4)):
+        with pytest.raises(ValueError):
+            oracle.ring_schedule(S, P)

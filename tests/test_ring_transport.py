@@ -166,3 +166,82 @@ def test_pins_catch_a_ring_running_backwards():
     with pytest.raises(AssertionError):
         for r in range(P):
             _check_rank(r, P, S, traces[r], bwd[r][1], bwd[r][2])
+
+
+def _check_rank_contiguous(rank, P, S, tr, dk, dv):
+    """The plain ring: the steps with work match the oracle's DIAG/FULL tasks,
+    and rank `rank`'s keys carry one mark from each rank at or after it."""
+    _, tasks = oracle.ring_schedule(S, P)
+    n = S // P
+    want = sorted((t for t in tasks if t["rank"] == rank and t["kind"] != oracle.TASK_NONE),
+                  key=lambda t: t["step"])
+    assert len(tr.fwd_seen) == len(want) == rank + 1 and len(tr.bwd_seen) == rank + 1
+    for t, f, b in zip(want, tr.fwd_seen, tr.bwd_seen):
+        assert f == (t["step"], t["src"], t["src"], t["kind"], t["q_off"] - rank * n, t["q_len"],
+                     t["k_off"] - t["src"] * n, t["k_len"], t["causal"]), (rank, f, t)
+        assert b == (t["step"], t["src"])
+    for other in range(P):
+        t = next(x for x in tasks if x["rank"] == other and x["src"] == rank)
+        has_work = t["kind"] != oracle.TASK_NONE
+        assert float(dk[0, 0, 0, other]) == (1.0 if has_work else 0.0)
+        assert float(dv[0, 0, 0, other]) == (1.0 + t["kind"] if has_work else 0.0)
+
+
+@pytest.mark.parametrize("P,n", [(1, 2), (2, 2), (3, 1), (4, 3), (8, 1)])
+def test_loopback_contiguous_ring_routes_kv_and_accumulators(P, n):
+    from long_context_causal_blockwise_gb300.ring import LoopbackRing, RingRank
+
+    S = P * n
+    hub = LoopbackRing(P)
+    traces = [TraceCompute(r) for r in range(P)]
+    ranks = [RingRank(r, P, S, hub.transport(r), compute=traces[r], schedule="contiguous") for r in range(P)]
+    data = [_local_n(r, n, P) for r in range(P)]
+    fwd = hub.run([rk.forward_steps(*data[r]) for r, rk in enumerate(ranks)])
+    bwd = hub.run([rk.backward_steps(*data[r], fwd[r][0], fwd[r][1], data[r][0]) for r, rk in enumerate(ranks)])
+    for r in range(P):
+        _check_rank_contiguous(r, P, S, traces[r], bwd[r][1], bwd[r][2])
+
+
+def _local_n(rank, n, P):
+    shape = (1, n, 1, max(P, 2))
+    return torch.zeros(shape), torch.full(shape, float(rank)), torch.full(shape, 100.0 + rank)
+
+
+def _gloo_rank_contiguous(rank, world, port, n, out):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from long_context_causal_blockwise_gb300.ring import DistRingTransport, RingRank, run_rank
+    from test_ring_transport import TraceCompute, _check_rank_contiguous, _local_n
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        S = world * n
+        tr = TraceCompute(rank)
+        rk = RingRank(rank, world, S, DistRingTransport(), compute=tr, schedule="contiguous")
+        q, k, v = _local_n(rank, n, world)
+        o, lse, _ = run_rank(rk.forward_steps(q, k, v))
+        dq, dk, dv = run_rank(rk.backward_steps(q, k, v, o, lse, q))
+        _check_rank_contiguous(rank, world, S, tr, dk, dv)
+        out.put((rank, "ok"))
+    except AssertionError as e:
+        out.put((rank, f"fail: {e}"))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_gloo_ranks_contiguous_ring():
+    world = 3
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gloo_rank_contiguous, args=(r, world, port, 2, out)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = sorted(out.get(timeout=180) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == [(r, "ok") for r in range(world)], got
