@@ -478,20 +478,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ahead): -LSE * log2(e) (-inf for a hidden or empty row) and
     // -scale * Delta; every thread reads all 32 through warp shuffles. The
     // arithmetic is the one-pass kernel's, so dK and dV match it bit for bit.
-    auto load_stats = [&](int i, float& l2v, float& dlv) {
+    // The raw values are loaded a whole step before their use; a query row
+    // past the block reads as LSE = -inf, Delta = 0.
+    float rl = 0.f, rd = 0.f;  // raw LSE and Delta of the next tile
+    auto fetch_stats = [&](int i) {
       const int q = (i0 + i) * kT + 32 * x + lane;
-      l2v = -lse2_of(p, b, h, q);
-      dlv = (q < p.Sq) ? -p.scale * __ldg(p.delta + b * p.l_bs + h * p.l_hs + q) : 0.f;
+      rl = q < p.Sq ? __ldg(p.lse + b * p.l_bs + h * p.l_hs + q) : -INFINITY;
+      rd = q < p.Sq ? __ldg(p.delta + b * p.l_bs + h * p.l_hs + q) : 0.f;
     };
-    float nl2 = 0.f, ndl = 0.f;
-    if (n > 0) load_stats(0, nl2, ndl);
+    if (n > 0) fetch_stats(0);
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
       const uint32_t ph = static_cast<uint32_t>(i) & 1u;
       const int it = i0 + i;            // query tile
       const int qx = it * kT + 32 * x;  // first query of this warpgroup's columns
-      const float l2v = nl2, dlv = ndl;
-      if (i + 1 < n) load_stats(i + 1, nl2, ndl);
+      const float l2v = (rl == -INFINITY) ? -INFINITY : -rl * kLog2e;  // fetched a step ago
+      const float dlv = -p.scale * rd;
+      if (i + 1 < n) fetch_stats(i + 1);
       ok = warp_all(mbar_wait(&bars->s_full, ph, abort_flag, p.st, kWhere | (5u << 16)));
       if (ok) ok = warp_all(mbar_wait(&bars->dp_full, ph, abort_flag, p.st, kWhere | (6u << 16)));
       if (!ok) break;
@@ -611,7 +614,8 @@ constexpr uint32_t kFuSmDo = kFuSmQ + kKvStages * kTileBytes;
 constexpr uint32_t kFuSmDs = kFuSmDo + kTileBytes;
 constexpr uint32_t kFuSmStg = kFuSmDs + kTileBytes;
 constexpr uint32_t kFuSmBar = kFuSmStg + 2 * kDqBlock;
-constexpr uint32_t kFuSmem = kFuSmBar + sizeof(Bars) + 1024;
+constexpr uint32_t kFuSmStats = kFuSmBar + ((sizeof(Bars) + 15) & ~15u);  // per-warpgroup row statistics, 1 KB
+constexpr uint32_t kFuSmem = kFuSmStats + 1024 + 1024;
 
 __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
@@ -814,21 +818,29 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint8_t* ds_tile = smem + kFuSmDs;
     uint8_t* stg_row = smem + kFuSmStg + (x & 1) * kDqBlock + row * 128;  // used by warpgroups 0 and 1
+    // This warpgroup's 32 query statistics of the current tile, published by
+    // every warp of the group (same values) and read back as broadcast float4s:
+    // -LSE * log2(e) for phase 1, -scale * Delta for phase 2. Each array is
+    // rewritten only after a barrier that every reader of its previous values
+    // has passed (s_full(s) needs all of phase 1 of tile s-1 done; dp_full(i)
+    // needs dq_free(i-1), which follows phase 2 of tile i-1 in every warp).
+    float* l2s = reinterpret_cast<float*>(smem + kFuSmStats) + 32 * x;
+    float* sds = reinterpret_cast<float*>(smem + kFuSmStats) + 128 + 32 * x;
     const int j = kt * kT + row;
     const bool key_ok = j < Sk;  // rows past the block's keys (zero-filled or another block's): P must be 0
     const float c = p.scale_log2;
-    // Lane l holds the statistics of query 32x + l of a tile (loaded a tile
-    // ahead): nl2 = -LSE * log2(e) (-inf for a hidden or empty row: P = 0) and
-    // nsd = -scale * Delta. Every thread reads all 32 through warp shuffles.
-    auto load_stats = [&](int i, float& nl2v, float& nsdv) {
+    // Lane l holds the statistics of query 32x + l of a tile: -LSE * log2(e)
+    // (-inf for a hidden or empty row: P = 0) and -scale * Delta. The raw
+    // values are loaded a whole step before their use, so no warp waits on
+    // the loads; a query row past the block reads as LSE = -inf, Delta = 0.
+    float rl = 0.f, rd = 0.f;  // raw LSE and Delta of the next tile
+    auto fetch_stats = [&](int i) {
       const int q = (i0 + i) * kT + 32 * x + lane;
       const long long si = b * p.l_bs + h * p.l_hs + q_off + q;
-      const float l = q < Sq ? __ldg(p.lse + si) : -INFINITY;
-      nl2v = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
-      nsdv = (q < Sq) ? -p.scale * __ldg(p.delta + si) : 0.f;
+      rl = q < Sq ? __ldg(p.lse + si) : -INFINITY;
+      rd = q < Sq ? __ldg(p.delta + si) : 0.f;
     };
-    float nl2 = 0.f, nsd = 0.f;
-    if (n > 0) load_stats(0, nl2, nsd);
+    if (n > 0) fetch_stats(0);
     bool ok = true;
     // Step s runs phase 2 of query tile s-1, phase 1 of tile s, then phase 3
     // of tile s-1: P^T(s) is computed while the tensor pipe runs dQ(s-1) and
@@ -847,18 +859,22 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         ok = warp_all(mbar_wait(&bars->dp_full, ph, abort_flag, p.st, kWhere | (6u << 16)));
         if (!ok) break;
         tc_fence_after();
+        sds[lane] = sd;
+        __syncwarp();
         uint32_t dk[16];
         {
           uint32_t dp[32];
           tmem_ld_x32(tDP + lane_off + 32 * x, dp);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float d0 = __shfl_sync(0xffffffffu, sd, e);
-            const float d1 = __shfl_sync(0xffffffffu, sd, e + 1);
+          for (int e = 0; e < 32; e += 4) {
+            const float4 d = *reinterpret_cast<const float4*>(sds + e);
             float t0, t1, u0, u1;
-            ffma2(t0, t1, __uint_as_float(dp[e]), __uint_as_float(dp[e + 1]), scl, scl, d0, d1);
+            ffma2(t0, t1, __uint_as_float(dp[e]), __uint_as_float(dp[e + 1]), scl, scl, d.x, d.y);
             fmul2(u0, u1, pv[e], pv[e + 1], t0, t1);
             dk[e >> 1] = pack_bf16x2(u0, u1);
+            ffma2(t0, t1, __uint_as_float(dp[e + 2]), __uint_as_float(dp[e + 3]), scl, scl, d.z, d.w);
+            fmul2(u0, u1, pv[e + 2], pv[e + 3], t0, t1);
+            dk[(e >> 1) + 1] = pack_bf16x2(u0, u1);
           }
         }
         if (i > 0) {
@@ -874,25 +890,29 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         // Phase 1: P^T(s), into this warpgroup's own S^T columns (already read by it).
         const int it = i0 + s;            // query tile
         const int qx = it * kT + 32 * x;  // first query of this warpgroup's columns
-        const float l2v = nl2;
-        sd = nsd;
-        if (s + 1 < n) load_stats(s + 1, nl2, nsd);
+        const float l2v = (rl == -INFINITY) ? -INFINITY : -rl * kLog2e;  // fetched a step ago
+        sd = -p.scale * rd;
+        if (s + 1 < n) fetch_stats(s + 1);
         ok = warp_all(mbar_wait(&bars->s_full, static_cast<uint32_t>(s) & 1u, abort_flag, p.st, kWhere | (5u << 16)));
         if (!ok) break;
         tc_fence_after();
+        l2s[lane] = l2v;
+        __syncwarp();
         // Only the diagonal tile and a ragged last key tile need a per-element mask.
         const bool masked = __any_sync(0xffffffffu, (causal && it == kt) || !key_ok);
         {
           uint32_t sv[32];
           tmem_ld_x32(tS + lane_off + 32 * x, sv);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float m0 = __shfl_sync(0xffffffffu, l2v, e);
-            const float m1 = __shfl_sync(0xffffffffu, l2v, e + 1);
+          for (int e = 0; e < 32; e += 4) {
+            const float4 m = *reinterpret_cast<const float4*>(l2s + e);
             float x0, x1;
-            ffma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), c, c, m0, m1);
+            ffma2(x0, x1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), c, c, m.x, m.y);
             pv[e] = ex2_approx(x0);
             pv[e + 1] = ex2_approx(x1);
+            ffma2(x0, x1, __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]), c, c, m.z, m.w);
+            pv[e + 2] = ex2_approx(x0);
+            pv[e + 3] = ex2_approx(x1);
           }
           if (masked) {
             const bool diag = causal && (it == kt);
