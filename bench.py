@@ -463,8 +463,9 @@ def run_e2e(args, world, dev, q, k, v, do, o, lse, dq, dk, dv):
     dev_out = [(torch.empty_like(o), torch.empty_like(lse), torch.empty_like(dq), torch.empty_like(dk),
                 torch.empty_like(dv)) for _ in range(2)]
     s_comp, s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    in_ready, in_free = [torch.cuda.Event() for _ in range(2)], [torch.cuda.Event() for _ in range(2)]
-    out_ready, out_free = [torch.cuda.Event() for _ in range(2)], [torch.cuda.Event() for _ in range(2)]
+    ev = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
+    # per buffer set: q, k, v in; dO in; inputs read; O, LSE ready; gradients ready; results out
+    qkv_in, do_in, in_free, fwd_out, bwd_out, out_free = ev(), ev(), ev(), ev(), ev(), ev()
 
     def e2e_run(nsteps):
         for i in range(nsteps):
@@ -473,20 +474,27 @@ def run_e2e(args, world, dev, q, k, v, do, o, lse, dq, dk, dv):
             o_, lse_, dq_, dk_, dv_ = dev_out[bi]
             s_h2d.wait_event(in_free[bi])  # step i-2 has finished reading this input set
             with torch.cuda.stream(s_h2d):
-                for d_, h_ in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo)):
+                for d_, h_ in ((q_, hq), (k_, hk), (v_, hv)):
                     d_.copy_(h_, non_blocking=True)
-                in_ready[bi].record(s_h2d)
-            s_comp.wait_event(in_ready[bi])
+                qkv_in[bi].record(s_h2d)
+                do_.copy_(hdo, non_blocking=True)  # only the backward reads dO
+                do_in[bi].record(s_h2d)
+            s_comp.wait_event(qkv_in[bi])
             s_comp.wait_event(out_free[bi])  # step i-2's results have left this output set
             with torch.cuda.stream(s_comp):
                 lcb.attn_fwd(q_, k_, v_, causal=True, scale=scale, o=o_, lse=lse_)
+                fwd_out[bi].record(s_comp)
+                s_comp.wait_event(do_in[bi])
                 lcb.attn_bwd(q_, k_, v_, o_, lse_, do_, causal=True, scale=scale, dq=dq_, dk=dk_, dv=dv_,
                              workspace=ws)
                 in_free[bi].record(s_comp)
-                out_ready[bi].record(s_comp)
-            s_d2h.wait_event(out_ready[bi])
+                bwd_out[bi].record(s_comp)
             with torch.cuda.stream(s_d2h):
-                for h_, d_ in ((ho, o_), (hlse, lse_), (hdq, dq_), (hdk, dk_), (hdv, dv_)):
+                s_d2h.wait_event(fwd_out[bi])  # O and LSE leave while the backward runs
+                for h_, d_ in ((ho, o_), (hlse, lse_)):
+                    h_.copy_(d_, non_blocking=True)
+                s_d2h.wait_event(bwd_out[bi])
+                for h_, d_ in ((hdq, dq_), (hdk, dk_), (hdv, dv_)):
                     h_.copy_(d_, non_blocking=True)
                 out_free[bi].record(s_d2h)
 
@@ -512,7 +520,8 @@ def run_e2e(args, world, dev, q, k, v, do, o, lse, dq, dk, dv):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_t, "steps": e2e_steps,
             "matches_device_run": same,
             "overlap": "step i+1's host-to-device and step i-1's device-to-host copies run on two copy "
-                       "streams during step i (double-buffered device tensors)"}
+                       "streams during step i (double-buffered device tensors); the forward starts once q, k, "
+                       "v are in, and O, LSE leave while the backward runs"}
 
 
 def size_record(h, s, steps, warmup, rope_theta, local_rank):
