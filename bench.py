@@ -145,6 +145,14 @@ def load_peaks():
         return {"burst": 1900.0, "sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
 
 
+def hbm_fields(prefix, nbytes, ms, peaks):
+    """Achieved GB/s of an HBM-bound call (algorithmic bytes over CUDA-event
+    milliseconds) and its fraction of the measured copy bandwidth."""
+    gbs = nbytes / ms / 1e6
+    return {prefix + "gbs": gbs, prefix + "frac_of_hbm": gbs / peaks["hbm"],
+            "hbm_peak": peaks["hbm"], "hbm_peak_source": peaks["source"]}
+
+
 def tensor_peak(peaks, timed_s, clocks):
     """The tensor peak that applies to a timed region: the burst figure (a
     short burst at full clocks), or the sustained one when the region ran for
@@ -812,12 +820,11 @@ def run_rope(args):
     t_fwd = timed(lambda: lcb.rope(x, theta), steps)
     t_inv = timed(lambda: lcb.rope(x, theta, inverse=True), steps)
     nbytes = 2 * x.numel() * 2  # read and write every element once
-    _, _, hbm, src = load_peaks()
+    pk = load_peaks()
     print(json.dumps({
         "metric": "RoPE (theta=1e6) on one bf16 [1, 524288, 32, 128] tensor, in place",
         "ms": t_fwd, "ms_inverse": t_inv, "bytes_per_call": nbytes,
-        "gbs": nbytes / t_fwd / 1e6, "gbs_inverse": nbytes / t_inv / 1e6,
-        "frac_of_hbm": nbytes / t_fwd / 1e6 / hbm, "hbm_peak": hbm, "hbm_peak_source": src,
+        **hbm_fields("", nbytes, t_fwd, pk), **hbm_fields("inverse_", nbytes, t_inv, pk),
         "inputs": "larger than L2 (4.3 GB); no flush"}), flush=True)
     return 0
 
@@ -860,13 +867,11 @@ def run_ce(args):
     t_fb = timed(lambda: lcb.cross_entropy(x, y, mode="fwd_bwd", loss=loss, lse=lse), steps)
     nb_fwd = N * V * 2 + N * (8 + 8)
     nb_fb = 2 * N * V * 2 + N * (8 + 8)
-    _, _, hbm, src = load_peaks()
+    pk = load_peaks()
     print(json.dumps({
         "metric": f"cross-entropy loss head, V={V}, N={N} tokens, bf16 logits",
         "fwd_bwd_ms": t_fb, "fwd_ms": t_fwd, "tokens_per_s_fwd_bwd": N / t_fb * 1e3,
-        "fwd_bwd_gbs": nb_fb / t_fb / 1e6, "fwd_gbs": nb_fwd / t_fwd / 1e6,
-        "fwd_bwd_frac_of_hbm": nb_fb / t_fb / 1e6 / hbm, "fwd_frac_of_hbm": nb_fwd / t_fwd / 1e6 / hbm,
-        "hbm_peak": hbm, "hbm_peak_source": src,
+        **hbm_fields("fwd_bwd_", nb_fb, t_fb, pk), **hbm_fields("fwd_", nb_fwd, t_fwd, pk),
         "inputs": "larger than L2 (2.1 GB of logits); no flush"}), flush=True)
     return 0
 

@@ -5,6 +5,7 @@ figure only while the kernel's sources still hash as they did at capture."""
 import os
 import sys
 
+import pytest
 import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -66,3 +67,16 @@ def test_load_peaks_reads_the_measured_file(tmp_path, monkeypatch):
         '{"hbm_gbs": 6743.6, "bf16_tflops": 1904.1, "bf16_tflops_sustained": 1715.4}')
     pk = bench.load_peaks()
     assert pk == {"burst": 1904.1, "sustained": 1715.4, "hbm": 6743.6, "source": "measured"}
+
+
+def test_hbm_fields_divide_by_the_measured_copy_bandwidth():
+    """The --rope and --ce lines: GB/s from algorithmic bytes and event ms, and
+    the fraction of the measured HBM copy figure, with its source named."""
+    peaks = {"burst": 1904.1, "sustained": 1715.4, "hbm": 6743.6, "source": "measured"}
+    rec = bench.hbm_fields("fwd_", 8.59e9, 1.5, peaks)
+    assert rec["fwd_gbs"] == pytest.approx(8.59e9 / 1.5e-3 / 1e9)
+    assert rec["fwd_frac_of_hbm"] == pytest.approx(rec["fwd_gbs"] / 6743.6)
+    assert rec["hbm_peak"] == 6743.6 and rec["hbm_peak_source"] == "measured"
+    # every mode of bench.py reads the peaks through the dict load_peaks returns
+    fb = bench.hbm_fields("", 1e9, 1.0, bench.load_peaks())
+    assert fb["frac_of_hbm"] > 0 and isinstance(fb["hbm_peak"], float)
