@@ -190,17 +190,22 @@ int launch_cross_entropy(void* logits, const long long* labels, float* loss, flo
                          int V, long long row_stride, int ignore_index, int mode, cudaStream_t stream) {
   __nv_bfloat16* x = static_cast<__nv_bfloat16*>(logits);
   const int vec = ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0) && (V % 8 == 0) && (row_stride % 8 == 0);
-  // 256-thread CTAs, four per SM: 608 rows in flight. With forward and
-  // backward in one call a row is read twice; when 608 rows exceed 64 MB (V
-  // above about 52000) one 1024-thread CTA per SM keeps the rows in flight,
-  // 152 of them, within L2 for the second read. The shape depends on V alone,
-  // so every mode reduces a row in the same order: the same loss and LSE bits.
-  if (4LL * kSms * V * 2 > (64LL << 20)) {
+  // 256-thread CTAs, five per SM (the most its 44 registers a thread allow):
+  // 760 rows in flight, the row-end reductions of one CTA covered by the
+  // loads of four others. With forward and backward in one call a row is read
+  // twice, so the rows in flight must stay within L2 (64 MB of it) for the
+  // second read: above that, four CTAs per SM (608 rows, V up to about 55000),
+  // then one 1024-thread CTA per SM (152 rows). The shape depends on V alone,
+  // and the order in which a row is reduced only on the CTA size, so every
+  // mode gives the same loss and LSE bits.
+  const long long row_bytes = 2LL * V;
+  if (4LL * kSms * row_bytes > (64LL << 20)) {
     const long long grid = std::min<long long>(N, kSms);
     ce_kernel<1024><<<static_cast<unsigned>(grid), 1024, 0, stream>>>(x, labels, loss, lse, dloss, N, V, row_stride,
                                                                       ignore_index, mode, vec);
   } else {
-    const long long grid = std::min<long long>(N, 4LL * kSms);
+    const long long per_sm = (5LL * kSms * row_bytes > (64LL << 20)) ? 4 : 5;
+    const long long grid = std::min<long long>(N, per_sm * kSms);
     ce_kernel<256><<<static_cast<unsigned>(grid), 256, 0, stream>>>(x, labels, loss, lse, dloss, N, V, row_stride,
                                                                     ignore_index, mode, vec);
   }

@@ -12,9 +12,13 @@
 //
 // One warp per token row (b, s): lane l owns pairs 2l and 2l + 1, computes
 // their two angles once and rotates them in every head, reading and writing
-// 4 bytes from each half of each head (a warp moves 256 contiguous bytes per
+// 4 bytes from each half of each head (a warp moves 128 contiguous bytes per
 // half-head). The kernel is bound by HBM: every element is read and written
-// once; in place is allowed.
+// once; in place is allowed. A call may be in place, so the compiler cannot
+// move one head's loads above the previous head's stores; the loads of eight
+// heads are therefore issued together before their stores (one head at a
+// time held about 256 bytes per warp in flight and reached 0.84 of the copy
+// bandwidth, eight reach 0.98).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -56,8 +60,26 @@ __global__ void __launch_bounds__(256) rope_kernel(const __nv_bfloat16* x, __nv_
     s0 *= sign;
     s1 *= sign;
     const long long row = b * bs + static_cast<long long>(s) * rs;
-    for (int h = 0; h < H; ++h) {
-      const long long lo = row + h * kD + 2 * lane;  // features 2l, 2l+1; their partners sit 64 further
+    int h = 0;
+    for (; h + 8 <= H; h += 8) {  // eight heads' loads in flight before their stores
+      uint32_t a[8], cc[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const long long lo = row + (h + u) * kD + 2 * lane;
+        a[u] = *reinterpret_cast<const uint32_t*>(x + lo);
+        cc[u] = *reinterpret_cast<const uint32_t*>(x + lo + kD / 2);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const long long lo = row + (h + u) * kD + 2 * lane;
+        const float a0 = bf16lo_to_f32(a[u]), a1 = bf16hi_to_f32(a[u]);
+        const float c0v = bf16lo_to_f32(cc[u]), c1v = bf16hi_to_f32(cc[u]);
+        *reinterpret_cast<uint32_t*>(y + lo) = pack_bf16x2(a0 * c0 - c0v * s0, a1 * c1 - c1v * s1);
+        *reinterpret_cast<uint32_t*>(y + lo + kD / 2) = pack_bf16x2(c0v * c0 + a0 * s0, c1v * c1 + a1 * s1);
+      }
+    }
+    for (; h < H; ++h) {
+      const long long lo = row + h * kD + 2 * lane;
       const uint32_t a = *reinterpret_cast<const uint32_t*>(x + lo);
       const uint32_t c = *reinterpret_cast<const uint32_t*>(x + lo + kD / 2);
       const float a0 = bf16lo_to_f32(a), a1 = bf16hi_to_f32(a);
