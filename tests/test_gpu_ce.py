@@ -41,15 +41,16 @@ def _check(x0, y, loss, lse, grad, rows=None, dloss=None):
         assert err.max() <= 1.0, err.max()
 
 
-@pytest.mark.parametrize("N,V", [(100, 1000), (37, 1001), (5, 8), (3, 1), (5000, 1000), (400, 57344), (40, 128256),
-                                 (9, 120001), (1, 128256)])
+@pytest.mark.parametrize("N,V", [(100, 1000), (37, 1001), (5, 8), (3, 1), (5000, 1000), (300, 50304), (400, 57344),
+                                 (40, 128256), (9, 120001), (1, 128256)])
 def test_ce_modes_vs_oracle(N, V):
     """fwd, fwd_bwd (in place) and bwd from a saved LSE. Rows are streamed
     through registers: 16-byte loads where a row's address and length are
-    multiples of 16 bytes (V = 1000, 8, 57344, 128256), one logit at a time
-    otherwise (V = 1001, 1, 120001); N = 5000 gives each persistent CTA many
-    rows; V = 57344 and above take the launch shape with one 1024-thread CTA
-    per SM."""
+    multiples of 16 bytes (V = 1000, 8, 50304, 57344, 128256), one logit at a
+    time otherwise (V = 1001, 1, 120001); N = 5000 gives each persistent CTA
+    many rows. The three launch shapes: five 256-thread CTAs per SM (V up to
+    about 44000), four (V = 50304), one 1024-thread CTA per SM (V = 57344 and
+    above)."""
     x, y = _case(N, V, seed=N + V)
     x0 = x.clone()
     loss, lse = lcb.cross_entropy(x, y, mode="fwd")

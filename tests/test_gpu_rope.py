@@ -43,6 +43,22 @@ def test_rope_matches_oracle(theta, pos0):
     assert np.abs(to64(back) - to64(x)).max() <= 2.0 ** -6 * np.abs(to64(x)).max()
 
 
+@pytest.mark.parametrize("H,in_place", [(8, False), (11, True), (32, True), (40, False)])
+def test_rope_head_batches_match_oracle(H, in_place):
+    """Head counts the kernel takes in batches of eight loads before their
+    stores (8, 32, 40) and with a remainder after them (11), in place and not:
+    every element within the bound of the fp64 rotation."""
+    g = torch.Generator(device="cuda").manual_seed(H)
+    x = torch.randn(1, 129, H, D, generator=g, device="cuda").to(torch.bfloat16)
+    want = oracle.rope(to64(x), 1e6, 4096)
+    x_before = to64(x)
+    y = lcb.rope(x, 1e6, 4096) if in_place else lcb.rope(x, 1e6, 4096, out=torch.empty_like(x))
+    torch.cuda.synchronize()
+    assert _rope_err(to64(y), want, x_before).max() <= 1.0
+    if in_place:
+        assert y.data_ptr() == x.data_ptr()
+
+
 def test_rope_strided_view_and_in_place():
     """Row strides wider than H*D (a q slice of a packed qkv buffer) and x == out."""
     g = torch.Generator(device="cuda").manual_seed(5)
