@@ -829,6 +829,46 @@ def run_rope(args):
     return 0
 
 
+def run_merge(args):
+    """Times the stand-alone LSE merge (attn_lse_merge) of one bf16 block into
+    the fp32 accumulator, 16384 rows x 32 heads x 128 (the ring step's merge at
+    S = 131072, P = 8), in place; L2 flushed between calls (each call is 0.68
+    GB, under L2 twice over); median of the timed calls. Prints one JSON line
+    (not the headline bench line)."""
+    import torch
+
+    import long_context_causal_blockwise_gb300 as lcb
+
+    Bm, Rm, Hm = 1, 16384, 32
+    dev = torch.device("cuda", 0)
+    lcb.load()
+    g = torch.Generator(device=dev).manual_seed(0)
+    o_acc = torch.randn(Bm, Rm, Hm, D, generator=g, device=dev)
+    lse_acc = torch.randn(Bm, Hm, Rm, generator=g, device=dev)
+    o_b = torch.randn(Bm, Rm, Hm, D, generator=g, device=dev).to(torch.bfloat16)
+    lse_b = torch.randn(Bm, Hm, Rm, generator=g, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        lcb.attn_lse_merge(o_acc, lse_acc, o_b, lse_b)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(max(3, min(args.steps, 20))):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        lcb.attn_lse_merge(o_acc, lse_acc, o_b, lse_b)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = statistics.median(ts)
+    nbytes = Bm * Rm * Hm * (D * (4 + 4 + 2) + 12)  # O_acc read and written, O_b read, statistics
+    print(json.dumps({
+        "metric": "LSE merge of a bf16 block into the fp32 accumulator, 16384 rows x 32 heads x 128, in place",
+        "ms": ms, "bytes_per_call": nbytes, **hbm_fields("", nbytes, ms, load_peaks()),
+        "inputs": "L2 flushed (256 MB written) before each timed call"}), flush=True)
+    return 0
+
+
 def run_ce(args):
     """Times the cross-entropy loss head, forward and in-place backward in one
     pass, on Llama-2's vocabulary (V = 32000) over a 32768-token sequence
@@ -891,6 +931,8 @@ def main():
     ap.add_argument("--H", type=int, default=H, help="heads (profiling of smaller cases only)")
     ap.add_argument("--S", type=int, default=S, help="sequence length (profiling of smaller cases only)")
     ap.add_argument("--vocab", type=int, default=32000, help="vocabulary size of --ce")
+    ap.add_argument("--merge", action="store_true",
+                    help="time the stand-alone LSE merge (attn_lse_merge) at the ring step's size and exit")
     ap.add_argument("--ce", action="store_true",
                     help="time the cross-entropy loss head (V=32000, 32768 tokens)")
     ap.add_argument("--rope", action="store_true",
@@ -906,6 +948,8 @@ def main():
         return run_zigzag(args)
     if args.rope:
         return run_rope(args)
+    if args.merge:
+        return run_merge(args)
     if args.ulysses:
         return run_ulysses(args)
     if args.ce:
