@@ -194,8 +194,10 @@ int attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int 
  * of disjoint key blocks add up to the monolithic gradient.
  * grad_mode LCB_GRAD_BF16: dq/dk/dv are bf16 and overwritten.
  * grad_mode LCB_GRAD_F32_ACCUM: dq/dk/dv are fp32 and the block's
- *   contribution is ADDED to them (read-modify-write; calls on one stream
- *   never race, calls on different streams touching the same rows do).
+ *   contribution is ADDED to them, each element by one fp32 atomic addition
+ *   in L2 (subnormal sums flush to zero): the kernel does not wait for the
+ *   old values, and contributions of calls on different streams to the same
+ *   rows add up too, in no fixed order.
  * grad_mode LCB_GRAD_F32_STORE: dq/dk/dv are fp32 and overwritten.
  * Gradient strides: dq uses dq_row/batch strides, dk and dv share dkv strides
  * (elements of the gradient dtype).

@@ -266,13 +266,15 @@ __device__ __forceinline__ void store_grad_chunk(void* base, long long off, cons
       float4 v = make_float4(__uint_as_float(a[i]) * mul, __uint_as_float(a[i + 1]) * mul,
                              __uint_as_float(a[i + 2]) * mul, __uint_as_float(a[i + 3]) * mul);
       if (mode == LCB_GRAD_F32_ACCUM) {
-        const float4 o = *reinterpret_cast<const float4*>(dst + i);
-        v.x += o.x;
-        v.y += o.y;
-        v.z += o.z;
-        v.w += o.w;
+        // Added in L2, fire and forget: the epilogue does not wait for the old value, which in a ring
+        // step's fp32 accumulator is rarely in L2. One CTA owns these rows in a launch, so the sum is
+        // the plain fp32 add (subnormal sums flush to zero, as the atomic add does).
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + i), "f"(v.x), "f"(v.y), "f"(v.z),
+                     "f"(v.w)
+                     : "memory");
+      } else {
+        *reinterpret_cast<float4*>(dst + i) = v;
       }
-      *reinterpret_cast<float4*>(dst + i) = v;
     }
   }
 }
